@@ -1,0 +1,200 @@
+/*
+ * attn_sink.h -- C ABI of a GB300 (sm_103a) library for attention with an
+ * attention sink.
+ *
+ * Two forms of the sink are implemented:
+ *
+ *  1. A learnable per-head sink logit (flash-attention PR "feat: Implement Sink
+ *     Attention", Description; sglang PR "openai oss attention sink support
+ *     with trtllm-gen backend", Summary of Changes).  For query head h the
+ *     value sink[h] is one extra logit that enters the softmax denominator and
+ *     carries no value vector:
+ *         m_i   = max(sink[h], max_j s_ij)
+ *         Z_i   = exp(sink[h] - m_i) + sum_j exp(s_ij - m_i)
+ *         O_i   = sum_j exp(s_ij - m_i) v_j / Z_i
+ *         LSE_i = m_i + ln Z_i
+ *     with s_ij = scale * q_i . k_j over the keys j that row i sees.  sink is
+ *     in the units of the scaled logits.  sink == NULL means "no sink"
+ *     (sink = -inf, i.e. plain softmax attention).
+ *
+ *  2. First-window + last-window KV selection over a paged KV cache (sglang PR
+ *     "To implement attention-sink", Motivation and the review's suggested
+ *     code: keep the first 1024 and the last 7168 tokens of every sequence).
+ *     A query at absolute position p sees the keys
+ *         [0, min(F, p+1))  U  [max(p+1-W, min(F, p+1)), p+1)
+ *     where F = win_first and W = win_last.  win_last <= 0 turns selection
+ *     off (plain causal).  The window is applied per sequence, token-exactly;
+ *     partial pages are masked per token.  Selection needs causal attention.
+ *
+ * Conventions shared by every entry point:
+ *  - Tensors are device pointers owned by the caller; the library keeps no
+ *    pointer after it returns.  Layouts are dense row-major as documented.
+ *  - bf16 tensors hold raw IEEE bfloat16 bits (attn_bf16).
+ *  - Work is queued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and is asynchronous: a zero return means "validated and
+ *    launched", not "finished".
+ *  - Query row t of a request with Lq queries and Lk keys sits at absolute
+ *    position Lk - Lq + t (bottom-right alignment: a cached prefix precedes
+ *    the new chunk).  A row that sees no key has O = 0 and LSE = sink (or
+ *    -inf without a sink); its gradients are 0.
+ *  - scale <= 0 selects 1/sqrt(head_dim).
+ *  - Scratch memory (split-KV partials, the fp32 dQ accumulator) is taken
+ *    from a library-owned stream-ordered pool on `stream` and returned on
+ *    the same stream; no call synchronises the host.
+ *  - Return values: ATTN_SINK_OK, or a negative status.  The text of the
+ *    last failure of the calling thread is available from
+ *    attn_sink_last_error().
+ *  - Out-of-range page ids and sequence lengths longer than the page table
+ *    are caught on the device: the offending load is skipped and a sticky
+ *    device status is set, which attn_sink_device_status() reports.
+ */
+#ifndef ATTN_SINK_H
+#define ATTN_SINK_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t attn_bf16;
+
+enum {
+    ATTN_SINK_OK = 0,
+    ATTN_SINK_ERR_INVALID = -1,      /* NULL pointer, negative size, bad flag combination */
+    ATTN_SINK_ERR_UNSUPPORTED = -2,  /* head_dim, group size or page_size not supported   */
+    ATTN_SINK_ERR_CUDA = -3,         /* a CUDA call failed (allocation, launch)            */
+    ATTN_SINK_ERR_DEVICE = -4        /* a device-side check failed (see device_status)     */
+};
+
+/* Device-side status bits reported by attn_sink_device_status(). */
+enum {
+    ATTN_SINK_DEV_PAGE_OOB = 1,      /* a page-table entry was outside [0, num_pages)       */
+    ATTN_SINK_DEV_SEQLEN_OOB = 2,    /* a sequence length exceeded max_pages * page_size    */
+    ATTN_SINK_DEV_TIMEOUT = 4        /* a pipeline wait ran out of time; the kernel gave up */
+};
+
+/*
+ * Forward attention with a sink over varlen requests (prefill, chunked
+ * extend, training forward).  Pages: flash-attention PR "feat: Implement Sink
+ * Attention" (Key Changes: forward functions and their variable-length
+ * counterparts take the sink); sglang PR "openai oss attention sink support with trtllm-gen backend" (Highlights: the extend path
+ * passes sink=).
+ *
+ *   q            (total_q, hq, head_dim) bf16, total_q = cu_seqlens_q[batch]
+ *   k, v         (total_k, hkv, head_dim) bf16; request b owns key rows
+ *                [cu_seqlens_k[b], cu_seqlens_k[b+1]) (cached prefix then chunk)
+ *   sink         (hq,) fp32 or NULL
+ *   cu_seqlens_q, cu_seqlens_k   (batch+1,) int32 device, non-decreasing, [0]=0
+ *   total_q, total_k             host row counts of q and k/v (the tensors'
+ *                first extents); cu_seqlens_*[batch] must not exceed them --
+ *                rows past them are never read or written and set
+ *                ATTN_SINK_DEV_SEQLEN_OOB
+ *   max_seqlen_q, max_seqlen_k   host upper bounds of the per-request lengths
+ *                (size the grid; no device-to-host read)
+ *   win_first, win_last          window selection (needs causal = 1)
+ *   out          (total_q, hq, head_dim) bf16
+ *   lse          (hq, total_q) fp32, natural log, includes the sink; may be NULL
+ * Supported: head_dim 64; hq % hkv == 0.  Key/value rows between requests
+ * must be finite (a tile may read its neighbour's rows and mask them).
+ */
+int attn_sink_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v,
+                  const float* sink, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                  int batch, int total_q, int total_k, int hq, int hkv, int head_dim,
+                  int max_seqlen_q, int max_seqlen_k,
+                  int win_first, int win_last, int causal, float scale,
+                  attn_bf16* out, float* lse, void* stream);
+
+/*
+ * Paged single-token decode with a sink and optional first/last-window
+ * selection.  Pages: sglang PR "openai oss attention sink support with trtllm-gen backend" (Highlights: the decode path passes
+ * sink=); sglang PR "To implement attention-sink" (page table rows built from the first and last
+ * windows, per sequence); flash-attention PR "feat: Implement Sink Attention" (a user reports the sink
+ * giving wrong decode results through the KV-cache API -- here the sink is
+ * folded exactly once, after the split-KV partials are merged).
+ *
+ *   q            (batch, hq, head_dim) bf16, one new token per request
+ *   k_cache, v_cache  (num_pages, page_size, hkv, head_dim) bf16
+ *   page_table   (batch, max_pages) int32 physical page ids; logical token t
+ *                of request b lives in page page_table[b][t / page_size],
+ *                row t % page_size.  Entries past a request's last page are
+ *                never read.
+ *   seqlens      (batch,) int32: cache length including the new token
+ *   sink         (hq,) fp32 or NULL
+ *   out          (batch, hq, head_dim) bf16
+ *   lse          (batch, hq) fp32 or NULL
+ * Supported: head_dim 64 or 128; hq % hkv == 0; page_size >= 1.
+ */
+int attn_sink_decode_paged(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_cache,
+                           const int32_t* page_table, int max_pages, const int32_t* seqlens,
+                           int batch, int hq, int hkv, int head_dim, int page_size, int num_pages,
+                           const float* sink, int win_first, int win_last, float scale,
+                           attn_bf16* out, float* lse, void* stream);
+
+/*
+ * Backward of attn_sink_fwd: gradients of sum(dout * out) with respect to q,
+ * k, v and the sink.  Page: flash-attention PR "feat: Implement Sink Attention" (Key Changes: the
+ * backward pass computes and returns the gradient of the learnable sink).
+ * dsink[h] = -sum_i exp(sink[h] - LSE_i) * rowsum(dout_i * out_i).
+ *
+ *   q, k, v, sink, cu_seqlens_*, sizes, windows, causal, scale: as in attn_sink_fwd
+ *   out, lse     the forward's outputs (lse is required here)
+ *   dout         (total_q, hq, head_dim) bf16
+ *   dq           (total_q, hq, head_dim) bf16
+ *   dk, dv       (total_k, hkv, head_dim) bf16 (summed over the query heads
+ *                of each KV head)
+ *   dsink        (hq,) fp32; must be non-NULL iff sink is non-NULL; written
+ *                (not accumulated)
+ * Supported: head_dim 64; hq % hkv == 0.
+ */
+int attn_sink_bwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, const float* sink,
+                  const attn_bf16* out, const float* lse, const attn_bf16* dout,
+                  const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                  int batch, int total_q, int total_k, int hq, int hkv, int head_dim,
+                  int max_seqlen_q, int max_seqlen_k,
+                  int win_first, int win_last, int causal, float scale,
+                  attn_bf16* dq, attn_bf16* dk, attn_bf16* dv, float* dsink, void* stream);
+
+/*
+ * The visible token ranges of each decode request, as the decode kernels
+ * compute them on the device (sglang PR "To implement attention-sink", suggested code: first window
+ * [:F] and last window [L-W:L], per sequence).
+ *   seqlens  (batch,) int32 device
+ *   ranges   (batch, 4) int32 device: a0, b0, a1, b1 with visible =
+ *            [a0,b0) U [a1,b1), disjoint and increasing.
+ */
+int attn_sink_visible_ranges(const int32_t* seqlens, int batch, int win_first, int win_last,
+                             int32_t* ranges, void* stream);
+
+/*
+ * The physical KV slot of every visible token, in the order the decode
+ * kernels read them: slot = page_table[b][t / page_size] * page_size
+ * + t % page_size for the visible logical tokens t of request b.
+ *   slots    (batch, max_visible) int32 device; row b holds the request's
+ *            visible slots followed by -1 padding (and -1 where a page id
+ *            is outside [0, num_pages), which also sets
+ *            ATTN_SINK_DEV_PAGE_OOB).  max_visible must be at least the
+ *            largest visible count.
+ */
+int attn_sink_visible_slots(const int32_t* seqlens, const int32_t* page_table, int max_pages,
+                            int batch, int page_size, int num_pages, int win_first, int win_last,
+                            int32_t* slots, int max_visible, void* stream);
+
+/*
+ * Reads and clears the sticky device status (a bitwise OR of the
+ * ATTN_SINK_DEV_* bits set by kernels since the last call) for the current
+ * device.  Synchronises `stream`.  Returns the bits, or ATTN_SINK_ERR_CUDA.
+ */
+int attn_sink_device_status(void* stream);
+
+/* Text of the calling thread's last failure ("" if none).  Never NULL. */
+const char* attn_sink_last_error(void);
+
+/* Library version string. */
+const char* attn_sink_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_SINK_H */

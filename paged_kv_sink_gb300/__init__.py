@@ -1,0 +1,17 @@
+"""Attention with an attention sink on GB300 (sm_103a).
+
+The compute path is the C-ABI library ``libattn_sink.so`` (hand-written CUDA
+kernels); this package holds its thin Python binding, the in-tree build
+script and the seeded synthetic workloads used by the tests and the bench.
+"""
+from ._lib import (  # noqa: F401
+    EXPORTS,
+    AttnSinkError,
+    attn_sink_bwd,
+    attn_sink_decode_paged,
+    attn_sink_fwd,
+    attn_sink_visible_ranges,
+    attn_sink_visible_slots,
+    device_status,
+    lib,
+)

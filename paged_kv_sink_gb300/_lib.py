@@ -1,0 +1,193 @@
+"""ctypes binding of libattn_sink.so (argument marshalling only).
+
+Every step of the computation runs in the library's CUDA kernels; this module
+only checks tensor dtypes/devices, allocates outputs with torch and passes raw
+pointers, sizes and the current CUDA stream through the C ABI.  There is no
+fallback: if the shared library is missing the import fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libattn_sink.so")
+
+OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE = 0, -1, -2, -3, -4
+DEV_PAGE_OOB, DEV_SEQLEN_OOB, DEV_TIMEOUT = 1, 2, 4
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+
+_SIGS = {
+    "attn_sink_fwd": [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P,
+                      _P],
+    "attn_sink_decode_paged": [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _I, _I, _F, _P, _P, _P],
+    "attn_sink_bwd": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I,
+                      _I, _F, _P, _P, _P, _P, _P],
+    "attn_sink_visible_ranges": [_P, _I, _I, _I, _P, _P],
+    "attn_sink_visible_slots": [_P, _P, _I, _I, _I, _I, _I, _I, _P, _I, _P],
+    "attn_sink_device_status": [_P],
+    "attn_sink_last_error": [],
+    "attn_sink_version": [],
+}
+
+EXPORTS = tuple(_SIGS)
+
+
+class AttnSinkError(RuntimeError):
+    def __init__(self, fn, code, msg):
+        super().__init__(f"{fn} returned {code}: {msg}")
+        self.code = code
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it first (python -m paged_kv_sink_gb300.build)")
+    lib = ctypes.CDLL(path)
+    for name, args in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_char_p if name in ("attn_sink_last_error", "attn_sink_version") else ctypes.c_int
+    return lib
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        _lib = load()
+    return _lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(name, rc):
+    if rc != OK:
+        msg = lib().attn_sink_last_error().decode()
+        raise AttnSinkError(name, rc, msg)
+
+
+def _need(t, dtype, name, dev=True):
+    if t is None:
+        return
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if dev and not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise TypeError(f"{name} must be contiguous")
+
+
+def attn_sink_fwd(q, k, v, sink, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                  win_first=0, win_last=0, causal=True, scale=0.0, out=None, lse=None,
+                  return_lse=True, stream=None):
+    """Varlen forward with a sink.  q (Tq,Hq,d), k/v (Tk,Hkv,d) bf16 CUDA; returns (out, lse)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, n)
+    _need(sink, torch.float32, "sink")
+    _need(cu_seqlens_q, torch.int32, "cu_seqlens_q")
+    _need(cu_seqlens_k, torch.int32, "cu_seqlens_k")
+    tq, hq, d = q.shape
+    hkv = k.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((hq, tq), dtype=torch.float32, device=q.device)
+    rc = lib().attn_sink_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(sink), _ptr(cu_seqlens_q),
+                             _ptr(cu_seqlens_k), cu_seqlens_q.numel() - 1, tq, k.shape[0], hq, hkv,
+                             d, int(max_seqlen_q), int(max_seqlen_k), int(win_first), int(win_last),
+                             1 if causal else 0, float(scale), _ptr(out), _ptr(lse), _stream(stream))
+    _check("attn_sink_fwd", rc)
+    return out, lse
+
+
+def attn_sink_decode_paged(q, k_cache, v_cache, page_table, seqlens, sink=None, win_first=0,
+                           win_last=0, scale=0.0, out=None, lse=None, return_lse=True, stream=None):
+    """Paged decode.  q (B,Hq,d); caches (P,ps,Hkv,d); page_table (B,maxp) int32; seqlens (B,)."""
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n)
+    _need(page_table, torch.int32, "page_table")
+    _need(seqlens, torch.int32, "seqlens")
+    _need(sink, torch.float32, "sink")
+    B, hq, d = q.shape
+    npages, ps, hkv, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, hq), dtype=torch.float32, device=q.device)
+    rc = lib().attn_sink_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table),
+                                      page_table.shape[1], _ptr(seqlens), B, hq, hkv, d, ps, npages,
+                                      _ptr(sink), int(win_first), int(win_last), float(scale),
+                                      _ptr(out), _ptr(lse), _stream(stream))
+    _check("attn_sink_decode_paged", rc)
+    return out, lse
+
+
+def attn_sink_bwd(q, k, v, sink, out, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
+                  max_seqlen_k, win_first=0, win_last=0, causal=True, scale=0.0, dq=None, dk=None,
+                  dv=None, dsink=None, stream=None):
+    """Backward with the sink's gradient; returns (dq, dk, dv, dsink or None)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        _need(t, torch.bfloat16, n)
+    _need(sink, torch.float32, "sink")
+    _need(lse, torch.float32, "lse")
+    tq, hq, d = q.shape
+    hkv = k.shape[1]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if sink is not None and dsink is None:
+        dsink = torch.empty_like(sink)
+    rc = lib().attn_sink_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(sink), _ptr(out), _ptr(lse), _ptr(dout),
+                             _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), cu_seqlens_q.numel() - 1, tq,
+                             k.shape[0], hq, hkv, d, int(max_seqlen_q), int(max_seqlen_k), int(win_first),
+                             int(win_last), 1 if causal else 0, float(scale), _ptr(dq), _ptr(dk),
+                             _ptr(dv), _ptr(dsink), _stream(stream))
+    _check("attn_sink_bwd", rc)
+    return dq, dk, dv, dsink
+
+
+def attn_sink_visible_ranges(seqlens, win_first, win_last, stream=None):
+    _need(seqlens, torch.int32, "seqlens")
+    B = seqlens.numel()
+    ranges = torch.empty((B, 4), dtype=torch.int32, device=seqlens.device)
+    rc = lib().attn_sink_visible_ranges(_ptr(seqlens), B, int(win_first), int(win_last),
+                                        _ptr(ranges), _stream(stream))
+    _check("attn_sink_visible_ranges", rc)
+    return ranges
+
+
+def attn_sink_visible_slots(seqlens, page_table, page_size, num_pages, win_first, win_last,
+                            max_visible, stream=None):
+    _need(seqlens, torch.int32, "seqlens")
+    _need(page_table, torch.int32, "page_table")
+    B = seqlens.numel()
+    slots = torch.empty((B, max_visible), dtype=torch.int32, device=seqlens.device)
+    rc = lib().attn_sink_visible_slots(_ptr(seqlens), _ptr(page_table), page_table.shape[1], B,
+                                       int(page_size), int(num_pages), int(win_first),
+                                       int(win_last), _ptr(slots), int(max_visible),
+                                       _stream(stream))
+    _check("attn_sink_visible_slots", rc)
+    return slots
+
+
+def device_status(stream=None) -> int:
+    rc = lib().attn_sink_device_status(_stream(stream))
+    if rc < 0:
+        _check("attn_sink_device_status", rc)
+    return rc

@@ -1,0 +1,297 @@
+// C ABI of the attention-with-sink library: argument validation, scratch
+// memory and kernel launches.  Every entry point is asynchronous on the
+// caller's stream and returns an ATTN_SINK_* status.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <mutex>
+#include <string>
+
+#include "attn_sink.h"
+#include "bwd.h"
+#include "common.cuh"
+#include "decode.h"
+#include "prefill.h"
+
+namespace {
+
+thread_local std::string t_last_error;
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(ATTN_SINK_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+// One library-owned stream-ordered memory pool per device.  Freed blocks are
+// kept (release threshold = max) so that steady-state calls do not go back to
+// the driver.
+constexpr int kMaxDevices = 64;
+std::mutex g_pool_mu;
+cudaMemPool_t g_pools[kMaxDevices] = {};
+
+cudaError_t device_pool(cudaMemPool_t* out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_pool_mu);
+    if (!g_pools[dev]) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool;
+        e = cudaMemPoolCreate(&pool, &props);
+        if (e != cudaSuccess) return e;
+        uint64_t thr = ~0ull;
+        e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &thr);
+        if (e != cudaSuccess) return e;
+        g_pools[dev] = pool;
+    }
+    *out = g_pools[dev];
+    return cudaSuccess;
+}
+
+// Stream-ordered scratch block, returned to the pool on the same stream.
+struct Scratch {
+    void* ptr = nullptr;
+    cudaStream_t stream = nullptr;
+    cudaError_t alloc(size_t bytes, cudaStream_t s) {
+        stream = s;
+        if (bytes == 0) return cudaSuccess;
+        cudaMemPool_t pool;
+        cudaError_t e = device_pool(&pool);
+        if (e != cudaSuccess) return e;
+        return cudaMallocFromPoolAsync(&ptr, bytes, pool, s);
+    }
+    ~Scratch() {
+        if (ptr) cudaFreeAsync(ptr, stream);
+    }
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+float resolve_scale(float scale, int head_dim) {
+    return scale > 0.f ? scale : 1.0f / sqrtf((float)head_dim);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_sink_last_error(void) { return t_last_error.c_str(); }
+
+const char* attn_sink_version(void) { return "attn_sink_gb300 0.1 (sm_103a)"; }
+
+int attn_sink_decode_paged(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_cache,
+                           const int32_t* page_table, int max_pages, const int32_t* seqlens,
+                           int batch, int hq, int hkv, int head_dim, int page_size, int num_pages,
+                           const float* sink, int win_first, int win_last, float scale,
+                           attn_bf16* out, float* lse, void* stream) {
+    t_last_error.clear();
+    if (batch < 0 || hq <= 0 || hkv <= 0 || max_pages <= 0 || page_size <= 0 || num_pages <= 0)
+        return fail(ATTN_SINK_ERR_INVALID, "decode: sizes must be positive (batch may be 0)");
+    if (win_first < 0) return fail(ATTN_SINK_ERR_INVALID, "decode: win_first must be >= 0");
+    if (head_dim != 64 && head_dim != 128)
+        return fail(ATTN_SINK_ERR_UNSUPPORTED, "decode: head_dim %d not supported (64, 128)", head_dim);
+    if (hq % hkv) return fail(ATTN_SINK_ERR_UNSUPPORTED, "decode: hq %% hkv != 0");
+    if (batch == 0) return ATTN_SINK_OK;
+    if (!q || !k_cache || !v_cache || !page_table || !seqlens || !out)
+        return fail(ATTN_SINK_ERR_INVALID, "decode: NULL tensor pointer");
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q) || !aligned16(out))
+        return fail(ATTN_SINK_ERR_INVALID, "decode: q, caches and out must be 16-byte aligned");
+    if ((long long)num_pages * page_size >= (1LL << 31) || (long long)max_pages * page_size >= (1LL << 31))
+        return fail(ATTN_SINK_ERR_UNSUPPORTED, "decode: cache slots must fit in int32");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    attn::decode::Args a;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.page_table = page_table;
+    a.seqlens = seqlens;
+    a.sink = sink;
+    a.out = out;
+    a.lse = lse;
+    a.max_pages = max_pages;
+    a.batch = batch;
+    a.hq = hq;
+    a.hkv = hkv;
+    a.head_dim = head_dim;
+    a.page_size = page_size;
+    a.num_pages = num_pages;
+    a.win_first = win_first;
+    a.win_last = win_last;
+    a.group = hq / hkv;
+    a.scale = resolve_scale(scale, head_dim);
+    attn::decode::Plan pl = attn::decode::make_plan(a);
+    Scratch ws;
+    cudaError_t e = ws.alloc(pl.part_o_bytes + pl.part_ml_bytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "decode: scratch allocation");
+    float* part_o = static_cast<float*>(ws.ptr);
+    float2* part_ml = reinterpret_cast<float2*>(static_cast<char*>(ws.ptr) + pl.part_o_bytes);
+    e = attn::decode::launch(a, pl, part_o, part_ml, s);
+    if (e != cudaSuccess) return cuda_fail(e, "decode: launch");
+    return ATTN_SINK_OK;
+}
+
+int attn_sink_visible_ranges(const int32_t* seqlens, int batch, int win_first, int win_last,
+                             int32_t* ranges, void* stream) {
+    t_last_error.clear();
+    if (batch < 0 || win_first < 0) return fail(ATTN_SINK_ERR_INVALID, "visible_ranges: bad sizes");
+    if (batch == 0) return ATTN_SINK_OK;
+    if (!seqlens || !ranges) return fail(ATTN_SINK_ERR_INVALID, "visible_ranges: NULL pointer");
+    cudaError_t e = attn::decode::launch_visible_ranges(seqlens, batch, win_first, win_last, ranges,
+                                                        static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "visible_ranges: launch");
+    return ATTN_SINK_OK;
+}
+
+int attn_sink_visible_slots(const int32_t* seqlens, const int32_t* page_table, int max_pages,
+                            int batch, int page_size, int num_pages, int win_first, int win_last,
+                            int32_t* slots, int max_visible, void* stream) {
+    t_last_error.clear();
+    if (batch < 0 || max_pages <= 0 || page_size <= 0 || num_pages <= 0 || max_visible < 0 || win_first < 0)
+        return fail(ATTN_SINK_ERR_INVALID, "visible_slots: bad sizes");
+    if ((long long)num_pages * page_size >= (1LL << 31))
+        return fail(ATTN_SINK_ERR_UNSUPPORTED, "visible_slots: cache slots must fit in int32");
+    if (batch == 0 || max_visible == 0) return ATTN_SINK_OK;
+    if (!seqlens || !page_table || !slots) return fail(ATTN_SINK_ERR_INVALID, "visible_slots: NULL pointer");
+    cudaError_t e = attn::decode::launch_visible_slots(seqlens, page_table, max_pages, batch, page_size,
+                                                       num_pages, win_first, win_last, slots, max_visible,
+                                                       static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "visible_slots: launch");
+    return ATTN_SINK_OK;
+}
+
+static int validate_varlen(const char* who, const void* q, const void* k, const void* v,
+                           const int32_t* cu_q, const int32_t* cu_k, int batch, int total_q,
+                           int total_k, int hq, int hkv,
+                           int head_dim, int max_seqlen_q, int max_seqlen_k, int win_first,
+                           int win_last, int causal) {
+    if (batch < 0 || total_q < 0 || total_k < 0 || hq <= 0 || hkv <= 0 || max_seqlen_q < 0 ||
+        max_seqlen_k < 0 || win_first < 0)
+        return fail(ATTN_SINK_ERR_INVALID, "%s: sizes must be non-negative (heads positive)", who);
+    if (win_last > 0 && !causal)
+        return fail(ATTN_SINK_ERR_INVALID, "%s: first/last-window selection needs causal attention", who);
+    if (head_dim != 64) return fail(ATTN_SINK_ERR_UNSUPPORTED, "%s: head_dim %d not supported (64)", who, head_dim);
+    if (hq % hkv) return fail(ATTN_SINK_ERR_UNSUPPORTED, "%s: hq %% hkv != 0", who);
+    if (batch == 0) return ATTN_SINK_OK;
+    if (!q || !k || !v || !cu_q || !cu_k) return fail(ATTN_SINK_ERR_INVALID, "%s: NULL tensor pointer", who);
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v))
+        return fail(ATTN_SINK_ERR_INVALID, "%s: q, k, v must be 16-byte aligned", who);
+    return ATTN_SINK_OK;
+}
+
+int attn_sink_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, const float* sink,
+                  const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch, int total_q,
+                  int total_k, int hq, int hkv, int head_dim, int max_seqlen_q, int max_seqlen_k,
+                  int win_first, int win_last, int causal, float scale, attn_bf16* out, float* lse,
+                  void* stream) {
+    t_last_error.clear();
+    int rc = validate_varlen("fwd", q, k, v, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, hq, hkv, head_dim,
+                             max_seqlen_q, max_seqlen_k, win_first, win_last, causal);
+    if (rc != ATTN_SINK_OK || batch == 0 || max_seqlen_q == 0 || total_q == 0) return rc;
+    if (!out) return fail(ATTN_SINK_ERR_INVALID, "fwd: NULL out");
+    if (!aligned16(out)) return fail(ATTN_SINK_ERR_INVALID, "fwd: out must be 16-byte aligned");
+    attn::prefill::FwdArgs a = {};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.sink = sink;
+    a.cu_q = cu_seqlens_q;
+    a.cu_k = cu_seqlens_k;
+    a.out = out;
+    a.lse = lse;
+    a.batch = batch;
+    a.total_q = total_q;
+    a.total_k = total_k;
+    a.hq = hq;
+    a.hkv = hkv;
+    a.head_dim = head_dim;
+    a.max_seqlen_q = max_seqlen_q;
+    a.max_seqlen_k = max_seqlen_k;
+    a.win_first = win_first;
+    a.win_last = win_last;
+    a.causal = causal ? 1 : 0;
+    a.scale = resolve_scale(scale, head_dim);
+    std::string err;
+    cudaError_t e = attn::prefill::launch_fwd(a, static_cast<cudaStream_t>(stream), &err);
+    if (e != cudaSuccess) return fail(ATTN_SINK_ERR_CUDA, "fwd: %s: %s", err.c_str(), cudaGetErrorString(e));
+    return ATTN_SINK_OK;
+}
+
+int attn_sink_bwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, const float* sink,
+                  const attn_bf16* out, const float* lse, const attn_bf16* dout,
+                  const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch, int total_q,
+                  int total_k, int hq, int hkv, int head_dim, int max_seqlen_q, int max_seqlen_k,
+                  int win_first, int win_last, int causal, float scale, attn_bf16* dq, attn_bf16* dk,
+                  attn_bf16* dv, float* dsink, void* stream) {
+    t_last_error.clear();
+    int rc = validate_varlen("bwd", q, k, v, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, hq, hkv, head_dim,
+                             max_seqlen_q, max_seqlen_k, win_first, win_last, causal);
+    if (rc != ATTN_SINK_OK) return rc;
+    if ((sink == nullptr) != (dsink == nullptr))
+        return fail(ATTN_SINK_ERR_INVALID, "bwd: dsink must be given exactly when sink is");
+    if (batch == 0) return ATTN_SINK_OK;
+    if (!out || !lse || !dout || !dq || !dk || !dv)
+        return fail(ATTN_SINK_ERR_INVALID, "bwd: NULL tensor pointer");
+    if (!aligned16(out) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return fail(ATTN_SINK_ERR_INVALID, "bwd: tensors must be 16-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    attn::bwd::Args a = {};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.sink = sink;
+    a.out = out;
+    a.lse = lse;
+    a.dout = dout;
+    a.cu_q = cu_seqlens_q;
+    a.cu_k = cu_seqlens_k;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.dsink = dsink;
+    a.batch = batch;
+    a.total_q = total_q;
+    a.total_k = total_k;
+    a.hq = hq;
+    a.hkv = hkv;
+    a.head_dim = head_dim;
+    a.max_seqlen_q = max_seqlen_q;
+    a.max_seqlen_k = max_seqlen_k;
+    a.win_first = win_first;
+    a.win_last = win_last;
+    a.causal = causal ? 1 : 0;
+    a.scale = resolve_scale(scale, head_dim);
+    size_t ws_bytes = attn::bwd::workspace_bytes(a);
+    Scratch ws;
+    cudaError_t e = ws.alloc(ws_bytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "bwd: scratch allocation");
+    std::string err;
+    e = attn::bwd::launch(a, ws.ptr, ws_bytes, s, &err);
+    if (e != cudaSuccess) return fail(ATTN_SINK_ERR_CUDA, "bwd: %s: %s", err.c_str(), cudaGetErrorString(e));
+    return ATTN_SINK_OK;
+}
+
+int attn_sink_device_status(void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int bits = 0;
+    int e = attn::decode::status_exchange(s, &bits);
+    if (!e) e = attn::prefill::status_exchange(s, &bits);
+    if (!e) e = attn::bwd::status_exchange(s, &bits);
+    if (e) return cuda_fail(static_cast<cudaError_t>(e), "device_status");
+    return bits;
+}
+
+}  // extern "C"

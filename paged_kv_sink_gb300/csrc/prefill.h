@@ -1,0 +1,30 @@
+// Host interface of the varlen forward kernel (prefill_fwd.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+namespace attn {
+namespace prefill {
+
+// Validated arguments of attn_sink_fwd.
+struct FwdArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* sink;
+    const int32_t* cu_q;
+    const int32_t* cu_k;
+    void* out;
+    float* lse;
+    int batch, total_q, total_k, hq, hkv, head_dim, max_seqlen_q, max_seqlen_k, win_first, win_last, causal;
+    float scale;
+};
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s, std::string* what);
+int status_exchange(cudaStream_t s, int* host_bits);
+
+}  // namespace prefill
+}  // namespace attn
