@@ -1,0 +1,461 @@
+"""Throughput of attention with an attention sink on GB300, against its roofline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload extend_varlen] [--no-extra]
+
+Prints ONE JSON line (rank 0).  The headline workload is the varlen chunked
+extend with a learnable sink (8 requests, prefix U{0..16384} + chunk
+U{512..8192}, Hq 64, Hkv 8, d 64): one step = one attn_sink_fwd call over the
+whole batch; the metric is algorithmic attention TFLOP/s (4*d FLOPs per
+visible (query, key) pair per head).  The decode workloads (HBM-bound, KV
+GB/s) and the training step (forward + backward TFLOP/s) are measured in the
+same run and reported under "workloads" with their own rooflines.
+
+Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
+on the stream the library launches on; L2 is flushed (a 512 MB write) before
+every timed step, outside the events.  Multi-GPU (torchrun): every rank runs
+an independent replica (the path shards by request; no collective), the time
+is the max over ranks and the value the sum of all ranks' work.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic per launch of the dominant kernel, from `ncu` captures (see
+# profiles/).  Keyed by kernel + workload; each entry records the hash of the
+# kernel source it was measured on and is reported only while that source is
+# unchanged.
+NCU_TRAFFIC = {
+    # profiles/fwd_kernel_extend_varlen.md: 443.3 MB read + 259.6 MB written per launch
+    "fwd_kernel/extend_varlen": {"src": "2d8b5eeb1c0aa8df", "bytes": 702_900_736},
+}
+
+
+def _src_hash(name):
+    p = os.path.join(ROOT, "paged_kv_sink_gb300", "csrc", name)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def _traffic(key, src):
+    ent = NCU_TRAFFIC.get(key)
+    if not ent or ent["src"] != _src_hash(src):
+        return None
+    return ent["bytes"]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            out = dict(FALLBACK_PEAKS)
+            for k in out:
+                for cand in (k, k.replace("_gbs", "_GBps")):
+                    if cand in d and isinstance(d[cand], (int, float)):
+                        out[k] = float(d[cand])
+            return out, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# Work counts (algorithmic, from the definition)
+
+def fwd_flops(p):
+    """4*d FLOPs (QK^T and PV) per visible (query, key) pair per query head."""
+    import numpy as np
+    total = 0
+    for Lq, Lk in zip(p.seqlens_q, p.seqlens_k):
+        off = Lk - Lq
+        if p.win_last <= 0:
+            if p.causal:
+                pos = np.arange(Lq) + off
+                total += int(np.clip(pos + 1, 0, Lk).sum())
+            else:
+                total += Lq * Lk
+        else:
+            pos = np.arange(Lq) + off
+            n = np.clip(pos + 1, 0, None)
+            first = np.minimum(p.win_first, n)
+            last_begin = np.maximum(n - p.win_last, first)
+            total += int((first + (n - last_begin)).sum())
+    return 4.0 * p.head_dim * p.hq * total
+
+
+def _visible_counts(seqlens, F, W):
+    out = []
+    for L in seqlens:
+        if W <= 0:
+            out.append(L)
+        else:
+            first = min(F, L)
+            last_begin = max(L - W, first)
+            out.append(first + (L - last_begin))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+
+def _flush_buf(torch, dev):
+    return torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+
+def time_steps(torch, fn, steps, warmup, flush):
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    return times
+
+
+def bench_extend(torch, ext, dev, p, steps, warmup, flush, peaks, peak_src):
+    q, k, v = p.q.to(dev), p.k.to(dev), p.v.to(dev)
+    sink = p.sink.to(dev)
+    cq, ck = p.cu_seqlens_q.to(dev), p.cu_seqlens_k.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((p.hq, q.shape[0]), dtype=torch.float32, device=dev)
+
+    def step():
+        ext.attn_sink_fwd(q, k, v, sink, cq, ck, p.max_seqlen_q, p.max_seqlen_k, out=out, lse=lse)
+
+    times = time_steps(torch, step, steps, warmup, flush)
+    flops = fwd_flops(p)
+    ms = sum(times) / len(times)
+    achieved = flops / (ms * 1e-3) / 1e12
+    roof = {"kernel": "attn::prefill::fwd_kernel", "bound": "tensor", "achieved": achieved,
+            "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+            "peak_source": f"bf16 burst, {peak_src}",
+            "traffic": _traffic("fwd_kernel/extend_varlen", "prefill_fwd.cu"),
+            "algorithmic_flops_per_launch": flops}
+    return ms, flops, roof, times
+
+
+def e2e_extend(torch, ext, dev, p, steps, warmup):
+    """Same metric through the public call with host buffers: pinned host ->
+    device copies of every input, the forward, device -> host copies of O and
+    LSE, all inside the timed region."""
+    hq_ = [t.pin_memory() for t in (p.q, p.k, p.v, p.sink, p.cu_seqlens_q, p.cu_seqlens_k)]
+    dq_ = [torch.empty_like(t, device=dev) for t in hq_]
+    out_h = torch.empty_like(p.q).pin_memory()
+    lse_h = torch.empty((p.hq, p.q.shape[0]), dtype=torch.float32).pin_memory()
+    out_d = torch.empty_like(dq_[0])
+    lse_d = torch.empty((p.hq, p.q.shape[0]), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for h, d in zip(hq_, dq_):
+            d.copy_(h, non_blocking=True)
+        ext.attn_sink_fwd(dq_[0], dq_[1], dq_[2], dq_[3], dq_[4], dq_[5], p.max_seqlen_q, p.max_seqlen_k,
+                          out=out_d, lse=lse_d)
+        out_h.copy_(out_d, non_blocking=True)
+        lse_h.copy_(lse_d, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    h2d = sum(t.numel() * t.element_size() for t in hq_)
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    return ms, h2d, d2h
+
+
+def bench_decode(torch, ext, dev, dc, steps, warmup, flush, peaks, peak_src):
+    t = dict(q=dc.q.to(dev), kc=dc.k_cache.to(dev), vc=dc.v_cache.to(dev), pt=dc.page_table.to(dev),
+             sl=dc.seqlens.to(dev), sink=None if dc.sink is None else dc.sink.to(dev))
+    out = torch.empty_like(t["q"])
+    lse = torch.empty((dc.batch, dc.hq), dtype=torch.float32, device=dev)
+
+    def step():
+        ext.attn_sink_decode_paged(t["q"], t["kc"], t["vc"], t["pt"], t["sl"], t["sink"], dc.win_first,
+                                   dc.win_last, out=out, lse=lse)
+
+    times = time_steps(torch, step, steps, warmup, flush)
+    nvis = _visible_counts(dc.seqlens.tolist(), dc.win_first, dc.win_last)
+    kv_bytes = sum(nvis) * 2 * dc.hkv * dc.head_dim * 2
+    ms = sum(times) / len(times)
+    gbs = kv_bytes / (ms * 1e-3) / 1e9
+    del t
+    return {"metric": "decode KV GB/s", "value": gbs, "unit": "GB/s", "ms_per_step": ms,
+            "kv_bytes": kv_bytes,
+            "roofline": {"kernel": "attn::decode::decode_split_kernel + decode_combine_kernel (whole call)",
+                         "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "peak_source": peak_src,
+                         "traffic": _traffic(f"decode/{dc.name.split()[0]}", "decode.cu")}}
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline (the oracle as it stands, on a bounded sample)
+
+def _sample_pairs(p, b):
+    Lq, Lk = p.seqlens_q[b], p.seqlens_k[b]
+    return sum(max(0, min(Lk - Lq + i + 1, Lk)) for i in range(Lq))
+
+
+def cpu_baseline_extend(p, budget_s=15.0):
+    """Sample: every row of the longest request, query heads 0..n-1, n doubled
+    until the oracle run takes about a third of the budget."""
+    import numpy as np
+    from oracle import attn_sink_oracle as orc
+    threads = _blas_threads()
+    b = int(np.argmax(p.seqlens_q))
+    nh = 1
+    while True:
+        t0 = time.perf_counter()
+        orc.attn_fwd(p.q, p.k, p.v, p.sink, p.cu_seqlens_q, p.cu_seqlens_k, p.win_first, p.win_last,
+                     p.causal, p.scale, heads=range(nh), requests=[b])
+        elapsed = time.perf_counter() - t0
+        if elapsed > budget_s / 3 or nh >= p.hq:
+            break
+        nh = min(p.hq, nh * 2)
+    work = 4.0 * p.head_dim * nh * _sample_pairs(p, b)
+    return {"value": work / elapsed / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"fp64 numpy oracle, request {b} (all {p.seqlens_q[b]} rows), {nh} of {p.hq} "
+                      f"heads ({work/1e9:.1f} GFLOP) in {elapsed:.1f} s"}
+
+
+def cpu_baseline_decode(dc, budget_s=10.0):
+    from oracle import attn_sink_oracle as orc
+    threads = _blas_threads()
+    n = 1
+    while True:
+        reqs = list(range(min(n, dc.batch)))
+        t0 = time.perf_counter()
+        orc.attn_decode_paged(dc.q, dc.k_cache, dc.v_cache, dc.page_table, dc.seqlens, dc.page_size,
+                              dc.sink, dc.win_first, dc.win_last, dc.scale, requests=reqs)
+        el = time.perf_counter() - t0
+        if el > budget_s / 3 or len(reqs) == dc.batch:
+            break
+        n *= 2
+    nvis = _visible_counts(dc.seqlens.tolist()[:len(reqs)], dc.win_first, dc.win_last)
+    b = sum(nvis) * 2 * dc.hkv * dc.head_dim * 2
+    return {"value": b / el / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"fp64 numpy oracle, {len(reqs)} of {dc.batch} requests, all heads, {el:.1f} s"}
+
+
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(k):
+            return int(os.environ[k])
+    return os.cpu_count()
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="extend_varlen")
+    ap.add_argument("--no-extra", action="store_true", help="skip the decode / training workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    import torch
+    from paged_kv_sink_gb300 import workloads as wl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        return reference_arm(args, wl)
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import paged_kv_sink_gb300 as ext
+    ext.lib()
+    peaks, peak_src = load_peaks()
+    flush = _flush_buf(torch, dev)
+
+    p = wl.workload(args.workload, seed=rank)
+    with ClockSampler(local) as clk:
+        ms, flops, roof, times = bench_extend(torch, ext, dev, p, args.steps, args.warmup, flush, peaks,
+                                              peak_src)
+    clocks = clk.summary()
+    e2e_ms, h2d, d2h = e2e_extend(torch, ext, dev, p, max(3, args.steps // 4), 2)
+
+    ms_max = ms
+    if dist is not None:
+        t = torch.tensor([ms, e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max, e2e_ms = float(t[0]), float(t[1])
+    value = flops * world / (ms_max * 1e-3) / 1e12
+    e2e_value = flops * world / (e2e_ms * 1e-3) / 1e12
+
+    extra = {}
+    if not args.no_extra:
+        for name in ("decode_sink", "decode_window"):
+            dc = wl.workload(name, seed=rank)
+            r = bench_decode(torch, ext, dev, dc, args.steps, args.warmup, flush, peaks, peak_src)
+            if rank == 0 and not args.no_cpu and world == 1:
+                r["cpu_baseline"] = cpu_baseline_decode(dc)
+            extra[name] = r
+            del dc
+
+    line = {
+        "metric": "attn TFLOP/s (prefill, fwd+bwd) & decode KV GB/s, % of GB300 roofline",
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_max,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; shapes and distributions of the varlen-extend workload)",
+        "config": {"workload": p.name, "requests": p.batch, "total_q": int(p.q.shape[0]),
+                   "total_k": int(p.k.shape[0]), "hq": p.hq, "hkv": p.hkv, "head_dim": p.head_dim,
+                   "causal": True, "l2": "flushed before every timed step (512 MB write)",
+                   "algorithmic_tflop_per_step": flops / 1e12},
+        "roofline": roof,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "workloads": extra,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline_extend(p)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+
+
+def reference_arm(args, wl):
+    """The oracle, as it stands, timed on the host cores: each step is a
+    bounded sample of the headline workload."""
+    p = wl.workload(args.workload)
+    from oracle import attn_sink_oracle as orc
+    import numpy as np
+    b = int(np.argmax(p.seqlens_q))
+    work = 4.0 * p.head_dim * _sample_pairs(p, b)
+    run = lambda: orc.attn_fwd(p.q, p.k, p.v, p.sink, p.cu_seqlens_q, p.cu_seqlens_k, p.win_first,
+                               p.win_last, p.causal, p.scale, heads=[0], requests=[b])
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    el = (time.perf_counter() - t0) / args.steps
+    value = work / el / 1e12
+    sample = f"fp64 numpy oracle, request {b} (all rows), head 0 ({work/1e9:.2f} GFLOP) per step"
+    print(json.dumps({
+        "impl": "reference",
+        "metric": "attn TFLOP/s (prefill, fwd+bwd) & decode KV GB/s, % of GB300 roofline",
+        "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "config": {"workload": p.name},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": _blas_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+if __name__ == "__main__":
+    main()
