@@ -132,6 +132,39 @@ int attn_sink_decode_paged(const attn_bf16* q, const attn_bf16* k_cache, const a
                            attn_bf16* out, float* lse, void* stream);
 
 /*
+ * Allocation-free paged decode.  The paper has no counterpart: this entry
+ * point exists for callers that cannot allocate device memory at call time
+ * (an engine that reserved the whole GPU up front, a latency-critical path
+ * that must not take the allocator's locks or its implicit synchronisation,
+ * a host that only hands the library existing buffers).
+ *
+ * Same arguments, semantics and results as attn_sink_decode_paged (up to
+ * rounding when it has to use longer splits), but its split-KV scratch lives
+ * in one static 32 MiB device array inside the library instead of coming
+ * from a memory pool.  It calls no cudaMalloc, cudaFree or other allocating
+ * routine.
+ *  - The array is shared by every call on a device and keeps the previous
+ *    call's contents; every scratch entry a call reads is written earlier in
+ *    the same call, so nothing needs clearing.  Calls whose work overlaps on
+ *    the GPU (e.g. on two streams without ordering between them) race on the
+ *    array: order them on one stream or with events.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) and caches it; make that first call before any
+ *    stream capture.
+ *  - A GPU holds the 32 MiB from the moment the library's module is loaded
+ *    on it until the process exits.
+ *  - Requests whose partials cannot fit in 32 MiB even with one split per
+ *    (request, head) -- batch * hq * (head_dim * 4 + 8) bytes -- are
+ *    rejected with ATTN_SINK_ERR_UNSUPPORTED and a message naming the size.
+ */
+int attn_sink_decode_paged_noalloc(const attn_bf16* q, const attn_bf16* k_cache,
+                                   const attn_bf16* v_cache, const int32_t* page_table,
+                                   int max_pages, const int32_t* seqlens, int batch, int hq,
+                                   int hkv, int head_dim, int page_size, int num_pages,
+                                   const float* sink, int win_first, int win_last, float scale,
+                                   attn_bf16* out, float* lse, void* stream);
+
+/*
  * Backward of attn_sink_fwd: gradients of sum(dout * out) with respect to q,
  * k, v and the sink.  Page: flash-attention PR "feat: Implement Sink Attention" (Key Changes: the
  * backward pass computes and returns the gradient of the learnable sink).

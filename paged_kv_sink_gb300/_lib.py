@@ -27,6 +27,8 @@ _SIGS = {
     "attn_sink_fwd": [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P,
                       _P],
     "attn_sink_decode_paged": [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _I, _I, _F, _P, _P, _P],
+    "attn_sink_decode_paged_noalloc": [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _I, _I, _F, _P,
+                                       _P, _P],
     "attn_sink_bwd": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I,
                       _I, _F, _P, _P, _P, _P, _P],
     "attn_sink_visible_ranges": [_P, _I, _I, _I, _P, _P],
@@ -117,7 +119,8 @@ def attn_sink_fwd(q, k, v, sink, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_s
 
 
 def attn_sink_decode_paged(q, k_cache, v_cache, page_table, seqlens, sink=None, win_first=0,
-                           win_last=0, scale=0.0, out=None, lse=None, return_lse=True, stream=None):
+                           win_last=0, scale=0.0, out=None, lse=None, return_lse=True, stream=None,
+                           _entry="attn_sink_decode_paged"):
     """Paged decode.  q (B,Hq,d); caches (P,ps,Hkv,d); page_table (B,maxp) int32; seqlens (B,)."""
     for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
         _need(t, torch.bfloat16, n)
@@ -130,12 +133,23 @@ def attn_sink_decode_paged(q, k_cache, v_cache, page_table, seqlens, sink=None, 
         out = torch.empty_like(q)
     if lse is None and return_lse:
         lse = torch.empty((B, hq), dtype=torch.float32, device=q.device)
-    rc = lib().attn_sink_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table),
-                                      page_table.shape[1], _ptr(seqlens), B, hq, hkv, d, ps, npages,
-                                      _ptr(sink), int(win_first), int(win_last), float(scale),
-                                      _ptr(out), _ptr(lse), _stream(stream))
-    _check("attn_sink_decode_paged", rc)
+    rc = getattr(lib(), _entry)(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table),
+                                page_table.shape[1], _ptr(seqlens), B, hq, hkv, d, ps, npages,
+                                _ptr(sink), int(win_first), int(win_last), float(scale),
+                                _ptr(out), _ptr(lse), _stream(stream))
+    _check(_entry, rc)
     return out, lse
+
+
+def attn_sink_decode_paged_noalloc(q, k_cache, v_cache, page_table, seqlens, sink=None, win_first=0,
+                                   win_last=0, scale=0.0, out=None, lse=None, return_lse=True,
+                                   stream=None):
+    """Allocation-free paged decode: the library allocates no device memory
+    for the call (its scratch is a static device array).  Outputs are still
+    allocated here by torch unless ``out``/``lse`` are given."""
+    return attn_sink_decode_paged(q, k_cache, v_cache, page_table, seqlens, sink, win_first, win_last,
+                                  scale, out, lse, return_lse, stream,
+                                  _entry="attn_sink_decode_paged_noalloc")
 
 
 def attn_sink_bwd(q, k, v, sink, out, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,

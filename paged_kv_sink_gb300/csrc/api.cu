@@ -87,6 +87,12 @@ float resolve_scale(float scale, int head_dim) {
 
 }  // namespace
 
+namespace attn {
+// Sets the calling thread's last-error text (used by entry points defined in
+// other translation units).
+void record_error(const char* msg) { t_last_error = msg; }
+}  // namespace attn
+
 extern "C" {
 
 const char* attn_sink_last_error(void) { return t_last_error.c_str(); }

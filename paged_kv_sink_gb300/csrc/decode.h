@@ -56,4 +56,7 @@ cudaError_t launch_visible_slots(const int32_t* seqlens, const int32_t* page_tab
 int status_exchange(cudaStream_t s, int* host_bits);
 
 }  // namespace decode
+
+void record_error(const char* msg);
+
 }  // namespace attn
