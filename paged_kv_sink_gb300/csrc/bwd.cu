@@ -1,12 +1,604 @@
+// Backward of varlen attention with a learnable sink (sm_103a).
+//
+// What it computes (flash-attention PR "feat: Implement Sink Attention", Key
+// Changes: the backward pass returns the gradient of the learnable sink):
+// with P_ij = e^{s_ij - LSE_i} over the visible keys and D_i = rowsum(dO_i o O_i)
+//     dS = P o (dO V^T - D),  dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO,
+//     dsink_h = -sum_i e^{sink_h - LSE_i} D_i
+// (the sink carries no value vector, so dO_i . dO/dsink = -p_sink,i D_i).
+//
+// Three kernels:
+//  * bwd_preprocess_kernel: D_i per (row, head) and dsink (warp shuffles, one
+//    fp32 atomic per block and head).
+//  * bwd_main_kernel (tcgen05): one CTA per (128-key tile, KV head, request);
+//    it loops over the query heads of the KV group and the 128-row query tiles
+//    that see its keys.  Per step five tcgen05 GEMMs:
+//        S^T = K Q^T, dP^T = V dO^T          (TMEM, 128 x 128 fp32 each)
+//        dV += P^T dO, dK += dS^T Q          (TMEM accumulators over the whole loop)
+//        dQ  = dS K                          (TMEM, double-buffered)
+//    P^T and dS^T are written by the softmax warpgroup to shared memory in the
+//    128-byte-swizzled layout; dS^T is read K-major for dK and MN-major (as dS)
+//    for dQ.  dK/dV are summed over the group in TMEM (no atomics); dQ is
+//    added to an fp32 accumulator with 16-byte vector atomics by a dedicated
+//    warpgroup.
+//  * bwd_dq_convert_kernel: fp32 dQ accumulator -> bf16.
+#include <cudaTypedefs.h>
+
 #include "bwd.h"
 #include "common.cuh"
+#include "sm103.cuh"
+
 namespace attn {
 namespace bwd {
-size_t workspace_bytes(const Args&) { return 0; }
-cudaError_t launch(const Args&, void*, size_t, cudaStream_t, std::string* what) {
-    *what = "not built yet";
-    return cudaErrorNotSupported;
+
+using namespace sm103;
+
+constexpr int BM = 128;  // query rows per tile
+constexpr int BN = 128;  // keys per CTA
+constexpr int D = 64;
+constexpr int kThreads = 384;
+constexpr int kRegsCtrl = 56;
+constexpr int kRegsWork = 224;  // 128*56 + 256*224 = 64512 = 384 * 168
+constexpr uint32_t kTile = 128 * 128;
+constexpr uint32_t kTmemCols = 512;
+// TMEM columns
+constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDK = 320, cDQ = 384;  // dQ: 384, 448
+
+struct __align__(1024) Smem {
+    uint8_t k[kTile];
+    uint8_t v[kTile];
+    uint8_t q[2][kTile];
+    uint8_t dout[2][kTile];
+    uint8_t pt[2 * kTile];   // P^T  (128 keys x 128 queries), two 64-query atoms
+    uint8_t dst[2 * kTile];  // dS^T (same layout)
+    float lse2[2][BM];       // LSE * log2(e) of the current query tile (+inf for rows past the end)
+    float dd[2][BM];         // D of the current query tile (0 past the end)
+    uint64_t kv_full;
+    uint64_t qdo_full[2], qdo_empty[2];
+    uint64_t sdp_full, sdp_free, pds_full, mma2_done;  // per step
+    uint64_t dq_full[2], dq_free[2];
+    uint64_t lse_ready[2];  // the softmax warpgroup has filled lse2/dd[buf]
+    uint64_t final_bar;
+    uint32_t tmem_base;
+    int abort;
+};
+
+struct MainParams {
+    const int32_t* cu_q;
+    const int32_t* cu_k;
+    const float* lse;      // (hq, total_q)
+    const float* dvec;     // (hq, total_q)
+    float* dq_accum;       // (total_q, hq, D) fp32
+    __nv_bfloat16* dk;     // (total_k, hkv, D)
+    __nv_bfloat16* dv;
+    int hq, hkv, group, total_q, total_k;
+    int win_first, win_last, causal;
+    float scale, scale_log2;
+};
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+    int dummy = 0;
+    mbar_wait(bar, parity, &dummy);
 }
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+// Query tiles of one head that see at least one key of [j0, j0 + BN).
+struct QRange {
+    int lo, hi;  // tile indices [lo, hi)
+};
+
+__device__ __forceinline__ QRange query_tiles(int j0, int Lq, int Lk, int causal, int F, int W) {
+    QRange r;
+    const int nqt = (Lq + BM - 1) / BM;
+    const int off = Lk - Lq;
+    int row_lo = 0, row_hi = Lq;  // query rows [row_lo, row_hi)
+    if (causal) row_lo = max(0, j0 - off);  // pos >= j0
+    if (W > 0 && j0 >= F) {
+        // keys all past the first window: pos + 1 - W <= j0 + BN - 1
+        row_hi = min(Lq, j0 + BN - 1 + W - off);
+    }
+    if (j0 >= Lk || row_lo >= row_hi) {
+        r.lo = r.hi = 0;
+        return r;
+    }
+    r.lo = row_lo / BM;
+    r.hi = min(nqt, (row_hi + BM - 1) / BM);
+    return r;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const MainParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kt = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+
+    const int q_start = p.cu_q[b];
+    int Lq = p.cu_q[b + 1] - q_start;
+    const int k_start = p.cu_k[b];
+    int Lk = p.cu_k[b + 1] - k_start;
+    if (q_start + Lq > p.total_q || k_start + Lk > p.total_k || Lq < 0 || Lk < 0) {
+        if (threadIdx.x == 0 && kt == 0 && kvh == 0) raise_status(ATTN_SINK_DEV_SEQLEN_OOB);
+        Lq = max(0, min(Lq, p.total_q - q_start));
+        Lk = max(0, min(Lk, p.total_k - k_start));
+    }
+    const int j0 = kt * BN;
+    if (j0 >= Lk) return;
+    const int off = Lk - Lq;
+    const QRange qr = query_tiles(j0, Lq, Lk, p.causal, p.win_first, p.win_last);
+    const int nqt = qr.hi - qr.lo;
+    const int T = nqt * p.group;  // steps: (head g, query tile)
+
+    if (threadIdx.x == 0) {
+        mbar_init(&S.kv_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&S.qdo_full[s], 1);
+            mbar_init(&S.qdo_empty[s], 1);
+            mbar_init(&S.dq_full[s], 1);
+            mbar_init(&S.dq_free[s], 128);
+            mbar_init(&S.lse_ready[s], 128);
+        }
+        mbar_init(&S.sdp_full, 1);
+        mbar_init(&S.sdp_free, 128);
+        mbar_init(&S.pds_full, 128);
+        mbar_init(&S.mma2_done, 1);
+        mbar_init(&S.final_bar, 1);
+        S.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&S.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = S.tmem_base;
+    volatile int* abort = &S.abort;
+
+    if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtrl));
+        if (warp == 0 && lane == 0) {
+            // -------------------------------------------------------- producer
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            prefetch_tmap(&tm_do);
+            mbar_expect_tx(&S.kv_full, 2 * kTile);
+            tma_load_3d(S.k, &tm_k, &S.kv_full, 0, kvh, k_start + j0);
+            tma_load_3d(S.v, &tm_v, &S.kv_full, 0, kvh, k_start + j0);
+            int t = 0;
+            for (; t < T; ++t) {
+                const int st = t & 1;
+                if (t >= 2 && !mbar_wait(&S.qdo_empty[st], ((t >> 1) - 1) & 1, abort)) break;
+                const int h = kvh * p.group + t / nqt;
+                const int q0 = (qr.lo + t % nqt) * BM;
+                mbar_expect_tx(&S.qdo_full[st], 2 * kTile);
+                tma_load_3d(S.q[st], &tm_q, &S.qdo_full[st], 0, h, q_start + q0);
+                tma_load_3d(S.dout[st], &tm_do, &S.qdo_full[st], 0, h, q_start + q0);
+            }
+            drain_wait(&S.kv_full, 0);
+            for (int st = 0; st < 2; ++st) {
+                const int n = t > st ? (t - st + 1) / 2 : 0;
+                if (n > 0) drain_wait(&S.qdo_full[st], (n - 1) & 1);
+            }
+        } else if (warp == 1 && lane == 0 && T > 0) {
+            // -------------------------------------------------------- MMA issuer
+            constexpr uint32_t idSS = idesc_bf16_f32(BN, BM, false, false);  // S^T, dP^T
+            constexpr uint32_t idKN = idesc_bf16_f32(BN, D, false, true);    // dV, dK: A K-major, B MN-major
+            constexpr uint32_t idQ = idesc_bf16_f32(BM, D, true, true);      // dQ: A (dS) MN-major, B (K) MN-major
+            const uint32_t sk = smem_u32(S.k), sv = smem_u32(S.v);
+            const uint32_t spt = smem_u32(S.pt), sds = smem_u32(S.dst);
+            auto issue_sdp = [&](int t) {
+                const uint32_t sq = smem_u32(S.q[t & 1]), sdo = smem_u32(S.dout[t & 1]);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    umma_ss(tmem + cS, sdesc_sw128(sk + kk * 32, 16, 1024), sdesc_sw128(sq + kk * 32, 16, 1024),
+                            idSS, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    umma_ss(tmem + cDP, sdesc_sw128(sv + kk * 32, 16, 1024),
+                            sdesc_sw128(sdo + kk * 32, 16, 1024), idSS, kk > 0);
+                umma_commit(&S.sdp_full);
+            };
+            bool ok = mbar_wait(&S.kv_full, 0, abort) && mbar_wait(&S.qdo_full[0], 0, abort);
+            if (ok) {
+                tc_fence_after();
+                issue_sdp(0);
+            }
+            for (int t = 0; ok && t < T; ++t) {
+                const int st = t & 1;
+                if (t + 1 < T) {
+                    // next step's S^T / dP^T as soon as the softmax has read this step's
+                    if (!(ok = mbar_wait(&S.qdo_full[(t + 1) & 1], ((t + 1) >> 1) & 1, abort))) break;
+                    if (!(ok = mbar_wait(&S.sdp_free, t & 1, abort))) break;
+                    tc_fence_after();
+                    issue_sdp(t + 1);
+                }
+                if (!(ok = mbar_wait(&S.pds_full, t & 1, abort))) break;
+                if (t >= 2 && !(ok = mbar_wait(&S.dq_free[st], ((t >> 1) - 1) & 1, abort))) break;
+                tc_fence_after();
+                const uint32_t sq = smem_u32(S.q[st]), sdo = smem_u32(S.dout[st]);
+#pragma unroll
+                for (int kk = 0; kk < BM / 16; ++kk) {
+                    const uint32_t koff = (kk >> 2) * kTile + (kk & 3) * 32;  // K-major step over queries
+                    const uint32_t moff = kk * 2048;                          // MN-major step over K rows
+                    const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
+                    umma_ss(tmem + cDV, sdesc_sw128(spt + koff, 16, 1024), sdesc_sw128(sdo + moff, 8192, 1024),
+                            idKN, acc);
+                    umma_ss(tmem + cDK, sdesc_sw128(sds + koff, 16, 1024), sdesc_sw128(sq + moff, 8192, 1024),
+                            idKN, acc);
+                }
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    umma_ss(tmem + cDQ + st * D, sdesc_sw128(sds + kk * 2048, kTile, 1024),
+                            sdesc_sw128(sk + kk * 2048, 8192, 1024), idQ, kk > 0);
+                umma_commit(&S.dq_full[st]);
+                umma_commit(&S.mma2_done);
+                umma_commit(&S.qdo_empty[st]);
+            }
+            umma_commit(&S.final_bar);
+            drain_wait(&S.final_bar, 0);
+        }
+    } else if (warp < 8) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsWork));
+        // ------------------------------------------------------------ P^T / dS^T
+        const int q4 = warp & 3;
+        const int j = q4 * 32 + lane;  // key row of this thread
+        const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+        const int kpos = j0 + j;
+        const float sl2 = p.scale_log2;
+        const int tid = threadIdx.x - 128;  // 0..127
+        bool ok = true;
+        for (int t = 0; t < T; ++t) {
+            const int g = t / nqt;
+            const int h = kvh * p.group + g;
+            const int q0 = (qr.lo + t % nqt) * BM;
+            const int buf = t & 1;
+            {  // this query tile's LSE (log2 units) and D
+                const int row = q0 + tid;
+                float l2 = INFINITY, dv = 0.f;
+                if (row < Lq) {
+                    l2 = p.lse[(size_t)h * p.total_q + q_start + row] * ATTN_LOG2E;
+                    dv = p.dvec[(size_t)h * p.total_q + q_start + row];
+                }
+                S.lse2[buf][tid] = l2;
+                S.dd[buf][tid] = dv;
+            }
+            mbar_arrive(&S.lse_ready[buf]);
+            ok = mbar_wait(&S.lse_ready[buf], (t >> 1) & 1, abort) && mbar_wait(&S.sdp_full, t & 1, abort);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int rows_valid = min(BM, Lq - q0);
+            const int P0 = off + q0, P1 = off + q0 + rows_valid - 1;
+            const int jmax = j0 + BN - 1;
+            const bool full = (!p.causal || jmax <= P0) && (jmax < Lk) &&
+                              (p.win_last <= 0 || jmax < p.win_first || j0 >= P1 + 1 - p.win_last);
+            // visible query columns of this key: c in [c_lo, c_hi]
+            const int c_lo = p.causal ? kpos - off - q0 : 0;
+            int c_hi = (p.win_last > 0 && kpos >= p.win_first) ? kpos - off - q0 + p.win_last - 1 : BM;
+            if (kpos >= Lk) c_hi = -1;
+            uint32_t pw[64], dw[64];  // packed bf16 P^T and dS^T of this key row
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t sr[32], dr[32];
+                tmem_ld32(tmem + lane_base + cS + ch * 32, sr);
+                tmem_ld32(tmem + lane_base + cDP + ch * 32, dr);
+                tmem_ld_wait();
+                if (ch == 3) {  // S^T / dP^T fully read: the next step may overwrite them
+                    tc_fence_before();
+                    mbar_arrive(&S.sdp_free);
+                }
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const int c = ch * 32 + i;
+                    float p0 = fast_exp2(fmaf(__uint_as_float(sr[i]), sl2, -S.lse2[buf][c]));
+                    float p1 = fast_exp2(fmaf(__uint_as_float(sr[i + 1]), sl2, -S.lse2[buf][c + 1]));
+                    if (!full) {
+                        if (c < c_lo || c > c_hi) p0 = 0.f;
+                        if (c + 1 < c_lo || c + 1 > c_hi) p1 = 0.f;
+                    }
+                    const float d0 = p0 * (__uint_as_float(dr[i]) - S.dd[buf][c]);
+                    const float d1 = p1 * (__uint_as_float(dr[i + 1]) - S.dd[buf][c + 1]);
+                    pw[(c >> 1)] = pack_bf16x2(p0, p1);
+                    dw[(c >> 1)] = pack_bf16x2(d0, d1);
+                }
+            }
+            if (t > 0) {  // the previous step's GEMMs must be done reading P^T / dS^T
+                ok = mbar_wait(&S.mma2_done, (t - 1) & 1, abort);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
+            }
+            // 128 queries = 16 chunks of 16 bytes: atom (cc >> 3), chunk (cc & 7)
+#pragma unroll
+            for (int cc = 0; cc < 16; ++cc) {
+                const uint32_t o = (cc >> 3) * kTile + sw128_off(j, cc & 7);
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(smem_u32(S.pt + o)), "r"(pw[4 * cc]),
+                             "r"(pw[4 * cc + 1]), "r"(pw[4 * cc + 2]), "r"(pw[4 * cc + 3])
+                             : "memory");
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(smem_u32(S.dst + o)), "r"(dw[4 * cc]),
+                             "r"(dw[4 * cc + 1]), "r"(dw[4 * cc + 2]), "r"(dw[4 * cc + 3])
+                             : "memory");
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&S.pds_full);
+        }
+        // ------------------------------------------------------------ dK, dV epilogue
+        if (ok && T > 0) ok = mbar_wait(&S.final_bar, 0, abort);
+        ok = __all_sync(0xffffffffu, ok);
+        const bool have = ok && T > 0;
+        if (have) tc_fence_after();
+        const size_t rowoff = ((size_t)(k_start + kpos) * p.hkv + kvh) * D;
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+            uint32_t u0[32], u1[32];
+            const uint32_t col = which == 0 ? cDK : cDV;
+            const float f = which == 0 ? p.scale : 1.f;
+            if (have) {  // warp-uniform: every lane takes part in the collective loads
+                tmem_ld32(tmem + lane_base + col, u0);
+                tmem_ld32(tmem + lane_base + col + 32, u1);
+                tmem_ld_wait();
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) u0[i] = u1[i] = 0u;
+            }
+            if (kpos < Lk) {
+                uint4* dst = reinterpret_cast<uint4*>((which == 0 ? p.dk : p.dv) + rowoff);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t* src = c < 4 ? u0 + 8 * c : u1 + 8 * (c - 4);
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(src[0]) * f, __uint_as_float(src[1]) * f);
+                    w.y = pack_bf16x2(__uint_as_float(src[2]) * f, __uint_as_float(src[3]) * f);
+                    w.z = pack_bf16x2(__uint_as_float(src[4]) * f, __uint_as_float(src[5]) * f);
+                    w.w = pack_bf16x2(__uint_as_float(src[6]) * f, __uint_as_float(src[7]) * f);
+                    dst[c] = w;
+                }
+            }
+        }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsWork));
+        // ------------------------------------------------------------ dQ epilogue
+        const int q4 = warp & 3;
+        const int r = q4 * 32 + lane;  // query row within the tile
+        const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+        for (int t = 0; t < T; ++t) {
+            const int st = t & 1;
+            const int h = kvh * p.group + t / nqt;
+            const int q0 = (qr.lo + t % nqt) * BM;
+            bool ok = mbar_wait(&S.dq_full[st], (t >> 1) & 1, abort);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            uint32_t u0[32], u1[32];
+            tmem_ld32(tmem + lane_base + cDQ + st * D, u0);
+            tmem_ld32(tmem + lane_base + cDQ + st * D + 32, u1);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(&S.dq_free[st]);
+            if (q0 + r < Lq) {
+                float* dst = p.dq_accum + ((size_t)(q_start + q0 + r) * p.hq + h) * D;
+                const float f = p.scale;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    red_add_v4(dst + 4 * c, __uint_as_float(u0[4 * c]) * f, __uint_as_float(u0[4 * c + 1]) * f,
+                               __uint_as_float(u0[4 * c + 2]) * f, __uint_as_float(u0[4 * c + 3]) * f);
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    red_add_v4(dst + 32 + 4 * c, __uint_as_float(u1[4 * c]) * f,
+                               __uint_as_float(u1[4 * c + 1]) * f, __uint_as_float(u1[4 * c + 2]) * f,
+                               __uint_as_float(u1[4 * c + 3]) * f);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// D_i = rowsum(dO_i o O_i) and dsink.  Block: 256 threads, 64 rows of one head;
+// 8 threads per row, 16 bytes each.
+
+__global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ out,
+                                                             const __nv_bfloat16* __restrict__ dout,
+                                                             const float* __restrict__ lse,
+                                                             const float* __restrict__ sink, float* __restrict__ dvec,
+                                                             float* __restrict__ dsink, int total_q, int hq) {
+    const int h = blockIdx.y;
+    const int tid = threadIdx.x;
+    const int sub = tid & 7;
+    const float sg = sink ? sink[h] : -INFINITY;
+    float acc_sink = 0.f;
+    for (int rr = 0; rr < 2; ++rr) {
+        const int row = blockIdx.x * 64 + rr * 32 + (tid >> 3);
+        float d = 0.f;
+        if (row < total_q) {
+            const size_t base = ((size_t)row * hq + h) * D + sub * 8;
+            const uint4 o = *reinterpret_cast<const uint4*>(out + base);
+            const uint4 g = *reinterpret_cast<const uint4*>(dout + base);
+            d = bf16_lo(o.x) * bf16_lo(g.x) + bf16_hi(o.x) * bf16_hi(g.x) + bf16_lo(o.y) * bf16_lo(g.y) +
+                bf16_hi(o.y) * bf16_hi(g.y) + bf16_lo(o.z) * bf16_lo(g.z) + bf16_hi(o.z) * bf16_hi(g.z) +
+                bf16_lo(o.w) * bf16_lo(g.w) + bf16_hi(o.w) * bf16_hi(g.w);
+        }
+        d += __shfl_xor_sync(0xffffffffu, d, 1);
+        d += __shfl_xor_sync(0xffffffffu, d, 2);
+        d += __shfl_xor_sync(0xffffffffu, d, 4);
+        if (row < total_q && sub == 0) {
+            dvec[(size_t)h * total_q + row] = d;
+            if (sink) {
+                const float l = lse[(size_t)h * total_q + row];
+                // probability mass on the sink, e^{sink - LSE}
+                float ps;
+                if (sg == -INFINITY)
+                    ps = 0.f;
+                else if (l == INFINITY)
+                    ps = 1.f;
+                else
+                    ps = __expf(sg - l);
+                acc_sink += -ps * d;
+            }
+        }
+    }
+    if (!sink) return;
+    for (int o = 16; o > 0; o >>= 1) acc_sink += __shfl_xor_sync(0xffffffffu, acc_sink, o);
+    __shared__ float red[8];
+    if ((tid & 31) == 0) red[tid >> 5] = acc_sink;
+    __syncthreads();
+    if (tid == 0) {
+        float s = 0.f;
+        for (int w = 0; w < 8; ++w) s += red[w];
+        atomicAdd(dsink + h, s);
+    }
+}
+
+__global__ void bwd_dq_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq, size_t n4) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+        const float4 v = acc[i];
+        dq[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+
+cudaError_t make_map(CUtensorMap* m, const void* base, int heads, long long rows, std::string* what);
+
+size_t workspace_bytes(const Args& a) {
+    const size_t acc = (size_t)a.total_q * a.hq * D * sizeof(float);
+    const size_t dv = (size_t)a.hq * a.total_q * sizeof(float);
+    return ((acc + 255) & ~size_t(255)) + dv;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+cudaError_t make_map(CUtensorMap* m, const void* base, int heads, long long rows, std::string* what) {
+    auto fn = encode_fn();
+    if (!fn) {
+        *what = "cuTensorMapEncodeTiled unavailable";
+        return cudaErrorNotSupported;
+    }
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1)};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)D * 2 * heads};
+    cuuint32_t box[3] = {(cuuint32_t)D, 1, 128};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        *what = "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")";
+        return cudaErrorInvalidValue;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch(const Args& a, void* workspace, size_t ws_bytes, cudaStream_t s, std::string* what) {
+    if (a.total_q == 0 && a.total_k == 0) return cudaSuccess;
+    cudaError_t e;
+    const size_t acc_bytes = (size_t)a.total_q * a.hq * D * sizeof(float);
+    float* dq_accum = static_cast<float*>(workspace);
+    float* dvec = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((acc_bytes + 255) & ~size_t(255)));
+    if (a.dsink && (e = cudaMemsetAsync(a.dsink, 0, sizeof(float) * a.hq, s)) != cudaSuccess) {
+        *what = "memset dsink";
+        return e;
+    }
+    // dK/dV rows of keys no CTA visits (past every request's end) are zero.
+    if ((e = cudaMemsetAsync(a.dk, 0, (size_t)a.total_k * a.hkv * D * 2, s)) != cudaSuccess ||
+        (e = cudaMemsetAsync(a.dv, 0, (size_t)a.total_k * a.hkv * D * 2, s)) != cudaSuccess) {
+        *what = "memset dk/dv";
+        return e;
+    }
+    if (a.total_q > 0) {
+        if ((e = cudaMemsetAsync(dq_accum, 0, acc_bytes, s)) != cudaSuccess) {
+            *what = "memset dq accumulator";
+            return e;
+        }
+        dim3 g1((a.total_q + 63) / 64, a.hq);
+        bwd_preprocess_kernel<<<g1, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(a.out),
+                                                 reinterpret_cast<const __nv_bfloat16*>(a.dout), a.lse, a.sink,
+                                                 dvec, a.dsink, a.total_q, a.hq);
+        if ((e = cudaGetLastError()) != cudaSuccess) {
+            *what = "preprocess launch";
+            return e;
+        }
+    }
+    if (a.total_q > 0 && a.total_k > 0 && a.max_seqlen_k > 0) {
+        CUtensorMap tq, tk, tv, tdo;
+        if ((e = make_map(&tq, a.q, a.hq, a.total_q, what)) != cudaSuccess) return e;
+        if ((e = make_map(&tk, a.k, a.hkv, a.total_k, what)) != cudaSuccess) return e;
+        if ((e = make_map(&tv, a.v, a.hkv, a.total_k, what)) != cudaSuccess) return e;
+        if ((e = make_map(&tdo, a.dout, a.hq, a.total_q, what)) != cudaSuccess) return e;
+        MainParams p;
+        p.cu_q = a.cu_q;
+        p.cu_k = a.cu_k;
+        p.lse = a.lse;
+        p.dvec = dvec;
+        p.dq_accum = dq_accum;
+        p.dk = reinterpret_cast<__nv_bfloat16*>(a.dk);
+        p.dv = reinterpret_cast<__nv_bfloat16*>(a.dv);
+        p.hq = a.hq;
+        p.hkv = a.hkv;
+        p.group = a.hq / a.hkv;
+        p.total_q = a.total_q;
+        p.total_k = a.total_k;
+        p.win_first = a.win_first;
+        p.win_last = a.win_last;
+        p.causal = a.causal;
+        p.scale = a.scale;
+        p.scale_log2 = a.scale * ATTN_LOG2E;
+        const size_t smem = sizeof(Smem) + 1024;
+        if ((e = cudaFuncSetAttribute(bwd_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+            cudaSuccess) {
+            *what = "smem attribute";
+            return e;
+        }
+        dim3 g2((a.max_seqlen_k + BN - 1) / BN, a.hkv, a.batch);
+        bwd_main_kernel<<<g2, kThreads, smem, s>>>(tq, tk, tv, tdo, p);
+        if ((e = cudaGetLastError()) != cudaSuccess) {
+            *what = "main launch";
+            return e;
+        }
+    }
+    if (a.total_q > 0) {
+        const size_t n4 = (size_t)a.total_q * a.hq * D / 4;
+        int blocks = (int)((n4 + 255) / 256);
+        if (blocks > 152 * 16) blocks = 152 * 16;
+        bwd_dq_convert_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(dq_accum),
+                                                    reinterpret_cast<uint2*>(a.dq), n4);
+        if ((e = cudaGetLastError()) != cudaSuccess) {
+            *what = "dq convert launch";
+            return e;
+        }
+    }
+    return cudaSuccess;
+}
+
 ATTN_DEFINE_STATUS_ACCESSOR(status_exchange)
+
 }  // namespace bwd
 }  // namespace attn

@@ -208,13 +208,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             for (int it = 0; ok && it < ntiles; ++it) {
                 const int nx = it + 1;
-                if (nx < ntiles && !(ok = mbar_wait(&S.kv_full[nx % NSTAGE], (nx / NSTAGE) & 1, abort))) break;
-                for (int s = 0; s < nslot && ok; ++s) {
-                    if (nx < ntiles) {
+                // Both heads' next S as soon as their softmax has read this S
+                // (it runs on the tensor core while the softmax works) ...
+                if (nx < ntiles) {
+                    if (!(ok = mbar_wait(&S.kv_full[nx % NSTAGE], (nx / NSTAGE) & 1, abort))) break;
+                    for (int s = 0; s < nslot && ok; ++s) {
                         if (!(ok = mbar_wait(&S.s_free[s], it & 1, abort))) break;
                         tc_fence_after();
                         issue_S(nx, s);
                     }
+                    if (!ok) break;
+                }
+                // ... then each head's P V once its P is in shared memory.
+                for (int s = 0; s < nslot && ok; ++s) {
                     if (!(ok = mbar_wait(&S.p_full[s], it & 1, abort))) break;
                     tc_fence_after();
                     issue_PV(it, s);
@@ -263,13 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int jmax = j0 + BN - 1;
                 const bool full = (!p.causal || jmax <= P0) && (jmax < Lk) &&
                                   (p.win_last <= 0 || jmax < p.win_first || j0 >= P1 + 1 - p.win_last);
-                float mx = -INFINITY;
-                if (full) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(s[c][i]));
-                } else {
+                if (!full) {
                     int c_hi = p.causal ? pos - j0 + 1 : BN;
                     c_hi = min(c_hi, Lk - j0);
                     const int f_hi = p.win_last > 0 ? p.win_first - j0 : BN;
@@ -280,11 +280,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int i = 0; i < 32; ++i) {
                             const int cc = c * 32 + i;
                             const bool vis = cc < c_hi && (cc < f_hi || cc >= w_lo);
-                            const float x = vis ? __uint_as_float(s[c][i]) : -INFINITY;
-                            s[c][i] = __float_as_uint(x);
-                            mx = fmaxf(mx, x);
+                            if (!vis) s[c][i] = __float_as_uint(-INFINITY);
                         }
                 }
+                // Row max: eight independent 3-input max chains of 16 values.
+                float mc[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t* v = &s[k >> 1][(k & 1) * 16];
+                    float m = max3f(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+#pragma unroll
+                    for (int i = 3; i < 15; i += 2) m = max3f(m, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+                    mc[k] = fmaxf(m, __uint_as_float(v[15]));
+                }
+                const float mx =
+                    max3f(max3f(mc[0], mc[1], mc[2]), max3f(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
                 const float m_new = fmaxf(m_ref, mx * sl2);
                 const bool resc = m_new > m_ref + kRescaleThreshold;
                 const float alpha = resc ? fast_exp2(m_ref - m_new) : 1.f;
@@ -322,22 +332,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                 }
-                float rs = 0.f;
+                // P = 2^(s*scale*log2e - m): packed fp32x2 FMA, MUFU ex2, packed partial sums.
+                const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(-m_use, -m_use);
+                uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
                 for (int cc = 0; cc < 16; ++cc) {
                     uint32_t w[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int i0 = cc * 8 + 2 * e;
-                        const float x0 = fast_exp2(fmaf(__uint_as_float(s[i0 >> 5][i0 & 31]), sl2, -m_use));
-                        const float x1 = fast_exp2(fmaf(__uint_as_float(s[(i0 + 1) >> 5][(i0 + 1) & 31]), sl2, -m_use));
-                        rs += x0 + x1;
+                        const uint64_t y = f2_fma(f2_pack(__uint_as_float(s[i0 >> 5][i0 & 31]),
+                                                          __uint_as_float(s[(i0 + 1) >> 5][(i0 + 1) & 31])),
+                                                  sc2, nm2);
+                        float y0, y1;
+                        f2_unpack(y, y0, y1);
+                        const float x0 = fast_exp2(y0), x1 = fast_exp2(y1);
+                        acc2[e] = f2_add(acc2[e], f2_pack(x0, x1));
                         w[e] = pack_bf16x2(x0, x1);
                     }
                     uint8_t* dst = prow + (cc >> 3) * kTile + sw128_off(r, cc & 7);
                     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(smem_u32(dst)), "r"(w[0]),
                                  "r"(w[1]), "r"(w[2]), "r"(w[3])
                                  : "memory");
+                }
+                float rs = 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float lo, hi;
+                    f2_unpack(acc2[e], lo, hi);
+                    rs += lo + hi;
                 }
                 l += rs;
                 fence_proxy_async_smem();
@@ -346,40 +369,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 
             // ---------------------------------------------------------- epilogue
-            float o[64];
             if (ok && ntiles > 0) ok = mbar_wait(&S.o_done[slot], (ntiles - 1) & 1, abort);
             ok = __all_sync(0xffffffffu, ok);
-            if (ok && ntiles > 0) {
-                tc_fence_after();
-                uint32_t u0[32], u1[32];
-                tmem_ld32(tO, u0);
-                tmem_ld32(tO + 32, u1);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    o[i] = __uint_as_float(u0[i]);
-                    o[32 + i] = __uint_as_float(u1[i]);
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 64; ++i) o[i] = 0.f;
-            }
+            const bool have = ok && ntiles > 0;
+            if (have) tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            const float lse_v = l > 0.f ? (m_ref + log2f(l)) * ATTN_LN2 : -INFINITY;
             const int row = q_start + qs + r;
-            if (r < rows_valid && ok) {
-                uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)row * p.hq + h) * D);
+            const bool store = r < rows_valid && ok;
+            uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)row * p.hq + h) * D);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint4 w;
-                    w.x = pack_bf16x2(o[8 * c + 0] * inv, o[8 * c + 1] * inv);
-                    w.y = pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
-                    w.z = pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
-                    w.w = pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
-                    dst[c] = w;
+            for (int half = 0; half < 2; ++half) {
+                uint32_t u[32];
+                if (have) {  // warp-uniform: every lane takes part in the collective load
+                    tmem_ld32(tO + half * 32, u);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) u[i] = 0u;
                 }
-                if (p.lse) p.lse[(size_t)h * p.total_q + row] = lse_v;
+                if (store) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(u[8 * c + 0]) * inv, __uint_as_float(u[8 * c + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(u[8 * c + 2]) * inv, __uint_as_float(u[8 * c + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(u[8 * c + 4]) * inv, __uint_as_float(u[8 * c + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(u[8 * c + 6]) * inv, __uint_as_float(u[8 * c + 7]) * inv);
+                        dst[half * 4 + c] = w;
+                    }
+                }
             }
+            if (store && p.lse) p.lse[(size_t)h * p.total_q + row] = l > 0.f ? (m_ref + log2f(l)) * ATTN_LN2 : -INFINITY;
         }
     }
 
