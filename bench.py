@@ -269,6 +269,57 @@ def bench_decode(torch, ext, dev, dc, steps, warmup, flush, peaks, peak_src):
                          "traffic": _traffic(f"decode/{dc.name.split()[0]}", "decode.cu")}}
 
 
+def bench_train(torch, ext, dev, p, steps, warmup, flush, peaks, peak_src):
+    """One training step = attn_sink_fwd + attn_sink_bwd over the whole batch.
+    FLOPs: forward 4*d per visible pair per head; backward 2.5x that (five
+    GEMMs including the recomputed S), the usual convention."""
+    q, k, v = p.q.to(dev), p.k.to(dev), p.v.to(dev)
+    sink, dout = p.sink.to(dev), p.dout.to(dev)
+    cq, ck = p.cu_seqlens_q.to(dev), p.cu_seqlens_k.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((p.hq, q.shape[0]), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dsink = torch.empty_like(sink)
+    stream = torch.cuda.current_stream()
+    fwd_ms, bwd_ms = [], []
+
+    def fwd():
+        ext.attn_sink_fwd(q, k, v, sink, cq, ck, p.max_seqlen_q, p.max_seqlen_k, out=out, lse=lse)
+
+    def bwd():
+        ext.attn_sink_bwd(q, k, v, sink, out, lse, dout, cq, ck, p.max_seqlen_q, p.max_seqlen_k, dq=dq, dk=dk,
+                          dv=dv, dsink=dsink)
+
+    for _ in range(warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    for _ in range(steps):
+        flush.zero_()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(stream)
+        fwd()
+        e[1].record(stream)
+        bwd()
+        e[2].record(stream)
+        torch.cuda.synchronize()
+        fwd_ms.append(e[0].elapsed_time(e[1]))
+        bwd_ms.append(e[1].elapsed_time(e[2]))
+    ff = fwd_flops(p)
+    bf = 2.5 * ff
+    fm, bm = sum(fwd_ms) / steps, sum(bwd_ms) / steps
+    total = (ff + bf) / ((fm + bm) * 1e-3) / 1e12
+    bw_ach = bf / (bm * 1e-3) / 1e12
+    return {"metric": "attn fwd+bwd TFLOP/s", "value": total, "unit": "TFLOP/s", "ms_per_step": fm + bm,
+            "fwd_ms": fm, "bwd_ms": bm, "fwd_tflops": ff / (fm * 1e-3) / 1e12, "bwd_tflops": bw_ach,
+            "algorithmic_tflop_per_step": (ff + bf) / 1e12,
+            "roofline": {"kernel": "attn_sink_bwd call (bwd_main_kernel + preprocess + dq convert)",
+                         "bound": "tensor", "achieved": bw_ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": bw_ach / peaks["bf16_tflops"], "peak_source": f"bf16 burst, {peak_src}",
+                         "traffic": _traffic("bwd_main_kernel/train", "bwd.cu"),
+                         "algorithmic_flops_per_launch": bf}}
+
+
 # ---------------------------------------------------------------------------
 # CPU baseline (the oracle as it stands, on a bounded sample)
 
@@ -343,6 +394,8 @@ def main():
     ap.add_argument("--workload", default="extend_varlen")
     ap.add_argument("--no-extra", action="store_true", help="skip the decode / training workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
+    ap.add_argument("--only", default=None, choices=["decode_sink", "decode_window", "train"],
+                    help="run one secondary workload alone and print its line (for profiling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -369,6 +422,16 @@ def main():
     peaks, peak_src = load_peaks()
     flush = _flush_buf(torch, dev)
 
+    if args.only:
+        w = wl.workload(args.only, seed=rank)
+        if args.only == "train":
+            r = bench_train(torch, ext, dev, w, args.steps, args.warmup, flush, peaks, peak_src)
+        else:
+            r = bench_decode(torch, ext, dev, w, args.steps, args.warmup, flush, peaks, peak_src)
+        if rank == 0:
+            print(json.dumps({"workload": w.name, **r}))
+        return
+
     p = wl.workload(args.workload, seed=rank)
     with ClockSampler(local) as clk:
         ms, flops, roof, times = bench_extend(torch, ext, dev, p, args.steps, args.warmup, flush, peaks,
@@ -393,6 +456,10 @@ def main():
                 r["cpu_baseline"] = cpu_baseline_decode(dc)
             extra[name] = r
             del dc
+        tr = wl.workload("train", seed=rank)
+        extra["train"] = bench_train(torch, ext, dev, tr, max(3, args.steps // 2), args.warmup, flush, peaks,
+                                     peak_src)
+        del tr
 
     line = {
         "metric": "attn TFLOP/s (prefill, fwd+bwd) & decode KV GB/s, % of GB300 roofline",
