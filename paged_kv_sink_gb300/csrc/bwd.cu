@@ -16,11 +16,12 @@
 //        S^T = K Q^T, dP^T = V dO^T          (TMEM, 128 x 128 fp32 each)
 //        dV += P^T dO, dK += dS^T Q          (TMEM accumulators over the whole loop)
 //        dQ  = dS K                          (TMEM, double-buffered)
-//    P^T and dS^T are written by the softmax warpgroup to shared memory in the
-//    128-byte-swizzled layout; dS^T is read K-major for dK and MN-major (as dS)
-//    for dQ.  dK/dV are summed over the group in TMEM (no atomics); dQ is
-//    added to an fp32 accumulator with 16-byte vector atomics by a dedicated
-//    warpgroup.
+//    Two warpgroups share the elementwise work: thread = (key row, half of the
+//    128 query columns).  They write P^T and dS^T to shared memory in the
+//    128-byte-swizzled layout (dS^T is read K-major for dK and MN-major, as dS,
+//    for dQ), and add the previous step's dQ tile (TMEM, double-buffered) to an
+//    fp32 accumulator with 16-byte vector atomics.  dK/dV are summed over the
+//    group in TMEM (no atomics).
 //  * bwd_dq_convert_kernel: fp32 dQ accumulator -> bf16.
 #include <cudaTypedefs.h>
 
@@ -37,8 +38,9 @@ constexpr int BM = 128;  // query rows per tile
 constexpr int BN = 128;  // keys per CTA
 constexpr int D = 64;
 constexpr int kThreads = 384;
-constexpr int kRegsCtrl = 56;
-constexpr int kRegsWork = 224;  // 128*56 + 256*224 = 64512 = 384 * 168
+constexpr int kRegsCtrl = 88;
+constexpr int kRegsWork = 208;  // 128*88 + 256*208 = 64512 = 384 * 168
+constexpr int kWork = 256;      // elementwise threads: warps 4..11
 constexpr uint32_t kTile = 128 * 128;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns
@@ -51,13 +53,13 @@ struct __align__(1024) Smem {
     uint8_t dout[2][kTile];
     uint8_t pt[2 * kTile];   // P^T  (128 keys x 128 queries), two 64-query atoms
     uint8_t dst[2 * kTile];  // dS^T (same layout)
-    float lse2[2][BM];       // LSE * log2(e) of the current query tile (+inf for rows past the end)
-    float dd[2][BM];         // D of the current query tile (0 past the end)
+    float nlse2[2][BM];      // -LSE * log2(e) of the current query tile (-inf for rows past the end)
+    float nd[2][BM];         // -D of the current query tile (0 past the end)
     uint64_t kv_full;
     uint64_t qdo_full[2], qdo_empty[2];
     uint64_t sdp_full, sdp_free, pds_full, mma2_done;  // per step
-    uint64_t dq_full[2], dq_free[2];
-    uint64_t lse_ready[2];  // the softmax warpgroup has filled lse2/dd[buf]
+    uint64_t dq_free[2];
+    uint64_t lse_ready[2];  // the elementwise warps have filled nlse2/nd[buf]
     uint64_t final_bar;
     uint32_t tmem_base;
     int abort;
@@ -140,13 +142,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < 2; ++s) {
             mbar_init(&S.qdo_full[s], 1);
             mbar_init(&S.qdo_empty[s], 1);
-            mbar_init(&S.dq_full[s], 1);
-            mbar_init(&S.dq_free[s], 128);
-            mbar_init(&S.lse_ready[s], 128);
+            mbar_init(&S.dq_free[s], kWork);
+            mbar_init(&S.lse_ready[s], kWork);
         }
         mbar_init(&S.sdp_full, 1);
-        mbar_init(&S.sdp_free, 128);
-        mbar_init(&S.pds_full, 128);
+        mbar_init(&S.sdp_free, kWork);
+        mbar_init(&S.pds_full, kWork);
         mbar_init(&S.mma2_done, 1);
         mbar_init(&S.final_bar, 1);
         S.abort = 0;
@@ -239,37 +240,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < BN / 16; ++kk)
                     umma_ss(tmem + cDQ + st * D, sdesc_sw128(sds + kk * 2048, kTile, 1024),
                             sdesc_sw128(sk + kk * 2048, 8192, 1024), idQ, kk > 0);
-                umma_commit(&S.dq_full[st]);
                 umma_commit(&S.mma2_done);
                 umma_commit(&S.qdo_empty[st]);
             }
             umma_commit(&S.final_bar);
             drain_wait(&S.final_bar, 0);
         }
-    } else if (warp < 8) {
+    } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsWork));
-        // ------------------------------------------------------------ P^T / dS^T
+        // ------------------------------------------------------------ elementwise
         const int q4 = warp & 3;
-        const int j = q4 * 32 + lane;  // key row of this thread
+        const int ch = (warp - 4) >> 2;      // query-column half: [64 ch, 64 ch + 64)
+        const int j = q4 * 32 + lane;        // key row (P^T/dS^T) and query row (dQ) of this lane
         const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
         const int kpos = j0 + j;
-        const float sl2 = p.scale_log2;
-        const int tid = threadIdx.x - 128;  // 0..127
+        const int tid = threadIdx.x - 128;   // 0..255
+        const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
         bool ok = true;
+
+        // dQ of step tt (its GEMMs are complete): 32 columns of this lane's query row.
+        auto flush_dq = [&](int tt) {
+            const int hh = kvh * p.group + tt / nqt;
+            const int qq0 = (qr.lo + tt % nqt) * BM;
+            uint32_t u[32];
+            tmem_ld32(tmem + lane_base + cDQ + (tt & 1) * D + ch * 32, u);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(&S.dq_free[tt & 1]);
+            if (qq0 + j < Lq) {
+                float* dst = p.dq_accum + ((size_t)(q_start + qq0 + j) * p.hq + hh) * D + ch * 32;
+                const float f = p.scale;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    red_add_v4(dst + 4 * c, __uint_as_float(u[4 * c]) * f, __uint_as_float(u[4 * c + 1]) * f,
+                               __uint_as_float(u[4 * c + 2]) * f, __uint_as_float(u[4 * c + 3]) * f);
+            }
+        };
+
         for (int t = 0; t < T; ++t) {
             const int g = t / nqt;
             const int h = kvh * p.group + g;
             const int q0 = (qr.lo + t % nqt) * BM;
             const int buf = t & 1;
-            {  // this query tile's LSE (log2 units) and D
-                const int row = q0 + tid;
-                float l2 = INFINITY, dv = 0.f;
-                if (row < Lq) {
-                    l2 = p.lse[(size_t)h * p.total_q + q_start + row] * ATTN_LOG2E;
-                    dv = p.dvec[(size_t)h * p.total_q + q_start + row];
-                }
-                S.lse2[buf][tid] = l2;
-                S.dd[buf][tid] = dv;
+            {  // this query tile's -LSE (log2 units) and -D: threads 0..127 / 128..255
+                const int c = tid & (BM - 1);
+                const int row = q0 + c;
+                if (tid < BM)
+                    S.nlse2[buf][c] = row < Lq ? -p.lse[(size_t)h * p.total_q + q_start + row] * ATTN_LOG2E
+                                               : -INFINITY;
+                else
+                    S.nd[buf][c] = row < Lq ? -p.dvec[(size_t)h * p.total_q + q_start + row] : 0.f;
             }
             mbar_arrive(&S.lse_ready[buf]);
             ok = mbar_wait(&S.lse_ready[buf], (t >> 1) & 1, abort) && mbar_wait(&S.sdp_full, t & 1, abort);
@@ -287,30 +307,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int c_lo = p.causal ? kpos - off - q0 : 0;
             int c_hi = (p.win_last > 0 && kpos >= p.win_first) ? kpos - off - q0 + p.win_last - 1 : BM;
             if (kpos >= Lk) c_hi = -1;
-            uint32_t pw[64], dw[64];  // packed bf16 P^T and dS^T of this key row
+            uint32_t pw[32], dw[32];  // packed bf16 P^T and dS^T of this key row, 64 query columns
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
+            for (int half = 0; half < 2; ++half) {
                 uint32_t sr[32], dr[32];
-                tmem_ld32(tmem + lane_base + cS + ch * 32, sr);
-                tmem_ld32(tmem + lane_base + cDP + ch * 32, dr);
+                const uint32_t col = ch * 64 + half * 32;
+                tmem_ld32(tmem + lane_base + cS + col, sr);
+                tmem_ld32(tmem + lane_base + cDP + col, dr);
                 tmem_ld_wait();
-                if (ch == 3) {  // S^T / dP^T fully read: the next step may overwrite them
+                if (half == 1) {  // S^T / dP^T fully read: the next step may overwrite them
                     tc_fence_before();
                     mbar_arrive(&S.sdp_free);
                 }
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
-                    const int c = ch * 32 + i;
-                    float p0 = fast_exp2(fmaf(__uint_as_float(sr[i]), sl2, -S.lse2[buf][c]));
-                    float p1 = fast_exp2(fmaf(__uint_as_float(sr[i + 1]), sl2, -S.lse2[buf][c + 1]));
+                    const int c = col + i;
+                    const uint64_t nl = *reinterpret_cast<const uint64_t*>(&S.nlse2[buf][c]);
+                    const uint64_t nd = *reinterpret_cast<const uint64_t*>(&S.nd[buf][c]);
+                    float y0, y1;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), sc2, nl), y0, y1);
+                    float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
                     if (!full) {
                         if (c < c_lo || c > c_hi) p0 = 0.f;
                         if (c + 1 < c_lo || c + 1 > c_hi) p1 = 0.f;
                     }
-                    const float d0 = p0 * (__uint_as_float(dr[i]) - S.dd[buf][c]);
-                    const float d1 = p1 * (__uint_as_float(dr[i + 1]) - S.dd[buf][c + 1]);
-                    pw[(c >> 1)] = pack_bf16x2(p0, p1);
-                    dw[(c >> 1)] = pack_bf16x2(d0, d1);
+                    const uint64_t p01 = f2_pack(p0, p1);
+                    const uint64_t ds =
+                        f2_mul(p01, f2_add(f2_pack(__uint_as_float(dr[i]), __uint_as_float(dr[i + 1])), nd));
+                    float d0, d1;
+                    f2_unpack(ds, d0, d1);
+                    pw[(half * 32 + i) >> 1] = pack_bf16x2(p0, p1);
+                    dw[(half * 32 + i) >> 1] = pack_bf16x2(d0, d1);
                 }
             }
             if (t > 0) {  // the previous step's GEMMs must be done reading P^T / dS^T
@@ -320,10 +347,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
             }
-            // 128 queries = 16 chunks of 16 bytes: atom (cc >> 3), chunk (cc & 7)
+            // 64 query columns = atom ch, chunks 0..7 of 16 bytes
 #pragma unroll
-            for (int cc = 0; cc < 16; ++cc) {
-                const uint32_t o = (cc >> 3) * kTile + sw128_off(j, cc & 7);
+            for (int cc = 0; cc < 8; ++cc) {
+                const uint32_t o = ch * kTile + sw128_off(j, cc);
                 asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(smem_u32(S.pt + o)), "r"(pw[4 * cc]),
                              "r"(pw[4 * cc + 1]), "r"(pw[4 * cc + 2]), "r"(pw[4 * cc + 3])
                              : "memory");
@@ -332,72 +359,51 @@ __global__ void __launch_bounds__(kThreads, 1)
                              : "memory");
             }
             fence_proxy_async_smem();
+            tc_fence_before();
             mbar_arrive(&S.pds_full);
+            if (t > 0) {
+                tc_fence_after();
+                flush_dq(t - 1);
+            }
         }
-        // ------------------------------------------------------------ dK, dV epilogue
+        // last step's dQ, then dK (column half 0) / dV (column half 1)
+        if (ok && T > 0) {
+            ok = mbar_wait(&S.mma2_done, (T - 1) & 1, abort);
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) {
+                tc_fence_after();
+                flush_dq(T - 1);
+            }
+        }
         if (ok && T > 0) ok = mbar_wait(&S.final_bar, 0, abort);
         ok = __all_sync(0xffffffffu, ok);
         const bool have = ok && T > 0;
         if (have) tc_fence_after();
         const size_t rowoff = ((size_t)(k_start + kpos) * p.hkv + kvh) * D;
+        const uint32_t col = ch == 0 ? cDK : cDV;
+        const float f = ch == 0 ? p.scale : 1.f;
+        __nv_bfloat16* outp = ch == 0 ? p.dk : p.dv;
 #pragma unroll
-        for (int which = 0; which < 2; ++which) {
-            uint32_t u0[32], u1[32];
-            const uint32_t col = which == 0 ? cDK : cDV;
-            const float f = which == 0 ? p.scale : 1.f;
+        for (int half = 0; half < 2; ++half) {
+            uint32_t u[32];
             if (have) {  // warp-uniform: every lane takes part in the collective loads
-                tmem_ld32(tmem + lane_base + col, u0);
-                tmem_ld32(tmem + lane_base + col + 32, u1);
+                tmem_ld32(tmem + lane_base + col + half * 32, u);
                 tmem_ld_wait();
             } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) u0[i] = u1[i] = 0u;
+                for (int i = 0; i < 32; ++i) u[i] = 0u;
             }
             if (kpos < Lk) {
-                uint4* dst = reinterpret_cast<uint4*>((which == 0 ? p.dk : p.dv) + rowoff);
+                uint4* dst = reinterpret_cast<uint4*>(outp + rowoff + half * 32);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint32_t* src = c < 4 ? u0 + 8 * c : u1 + 8 * (c - 4);
+                for (int c = 0; c < 4; ++c) {
                     uint4 w;
-                    w.x = pack_bf16x2(__uint_as_float(src[0]) * f, __uint_as_float(src[1]) * f);
-                    w.y = pack_bf16x2(__uint_as_float(src[2]) * f, __uint_as_float(src[3]) * f);
-                    w.z = pack_bf16x2(__uint_as_float(src[4]) * f, __uint_as_float(src[5]) * f);
-                    w.w = pack_bf16x2(__uint_as_float(src[6]) * f, __uint_as_float(src[7]) * f);
+                    w.x = pack_bf16x2(__uint_as_float(u[8 * c + 0]) * f, __uint_as_float(u[8 * c + 1]) * f);
+                    w.y = pack_bf16x2(__uint_as_float(u[8 * c + 2]) * f, __uint_as_float(u[8 * c + 3]) * f);
+                    w.z = pack_bf16x2(__uint_as_float(u[8 * c + 4]) * f, __uint_as_float(u[8 * c + 5]) * f);
+                    w.w = pack_bf16x2(__uint_as_float(u[8 * c + 6]) * f, __uint_as_float(u[8 * c + 7]) * f);
                     dst[c] = w;
                 }
-            }
-        }
-    } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsWork));
-        // ------------------------------------------------------------ dQ epilogue
-        const int q4 = warp & 3;
-        const int r = q4 * 32 + lane;  // query row within the tile
-        const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
-        for (int t = 0; t < T; ++t) {
-            const int st = t & 1;
-            const int h = kvh * p.group + t / nqt;
-            const int q0 = (qr.lo + t % nqt) * BM;
-            bool ok = mbar_wait(&S.dq_full[st], (t >> 1) & 1, abort);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            tc_fence_after();
-            uint32_t u0[32], u1[32];
-            tmem_ld32(tmem + lane_base + cDQ + st * D, u0);
-            tmem_ld32(tmem + lane_base + cDQ + st * D + 32, u1);
-            tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(&S.dq_free[st]);
-            if (q0 + r < Lq) {
-                float* dst = p.dq_accum + ((size_t)(q_start + q0 + r) * p.hq + h) * D;
-                const float f = p.scale;
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    red_add_v4(dst + 4 * c, __uint_as_float(u0[4 * c]) * f, __uint_as_float(u0[4 * c + 1]) * f,
-                               __uint_as_float(u0[4 * c + 2]) * f, __uint_as_float(u0[4 * c + 3]) * f);
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    red_add_v4(dst + 32 + 4 * c, __uint_as_float(u1[4 * c]) * f,
-                               __uint_as_float(u1[4 * c + 1]) * f, __uint_as_float(u1[4 * c + 2]) * f,
-                               __uint_as_float(u1[4 * c + 3]) * f);
             }
         }
     }

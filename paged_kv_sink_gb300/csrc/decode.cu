@@ -114,7 +114,6 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitParam
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int kStageBytes = 2 * kChunk * D * 2;
     constexpr int kSegs = D / 8;                        // 16-byte segments per row
-    constexpr int kPerThread = kChunk * kSegs / kThreads;
 
     const int split = blockIdx.x;
     const int kvh = blockIdx.y / p.hblocks;
@@ -146,33 +145,48 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitParam
         }
     }
 
+    // Loading: every warp instruction copies whole contiguous token rows
+    // (32 x 16 B = 512 B: four 128-byte rows at d 64, two 256-byte rows at
+    // d 128).  A warp stages 16 of the chunk's 64 rows; lanes 0..15 look up
+    // one row's physical slot each (one page-table read per row and chunk) and
+    // the copies fetch it by shuffle.
+    constexpr int kRowsPerInst = 32 / kSegs;          // rows per warp instruction
+    constexpr int kInsts = 16 / kRowsPerInst;         // instructions per warp and chunk
+    const int my_seg = lane % kSegs, my_sub = lane / kSegs;
     auto load_chunk = [&](int c, int stage) {
         uint8_t* sK = smem + stage * kStageBytes;
         uint8_t* sV = sK + kChunk * D * 2;
-#pragma unroll
-        for (int i = 0; i < kPerThread; ++i) {
-            const int seg = tid + i * kThreads;
-            const int row = seg / kSegs, col = seg % kSegs;
+        // slot of the warp's (lane)-th row; rows of instruction i: (i*4 + warp) * kRowsPerInst + sub
+        int slot = -1;
+        if (lane < 16) {
+            const int row = ((lane / kRowsPerInst) * 4 + warp) * kRowsPerInst + (lane % kRowsPerInst);
             const int v = v0 + c * kChunk + row;
-            const __nv_bfloat16* srcK = p.k_cache;
-            const __nv_bfloat16* srcV = p.v_cache;
-            int bytes = 0;
             if (v < v1) {
                 const int t = visible_token(r, v);
-                const int page = p.page_table[(size_t)b * p.max_pages + t / p.page_size];
-                if ((unsigned)page < (unsigned)p.num_pages) {
-                    const size_t off =
-                        (((size_t)page * p.page_size + (t % p.page_size)) * p.hkv + kvh) * D + col * 8;
-                    srcK += off;
-                    srcV += off;
-                    bytes = 16;
+                int pg, in_pg;
+                if (p.page_shift >= 0) {
+                    pg = t >> p.page_shift;
+                    in_pg = t & ((1 << p.page_shift) - 1);
                 } else {
-                    raise_status(ATTN_SINK_DEV_PAGE_OOB);
+                    pg = t / p.page_size;
+                    in_pg = t - pg * p.page_size;
                 }
+                const int page = p.page_table[(size_t)b * p.max_pages + pg];
+                if ((unsigned)page < (unsigned)p.num_pages)
+                    slot = page * p.page_size + in_pg;
+                else
+                    raise_status(ATTN_SINK_DEV_PAGE_OOB);
             }
-            const uint32_t so = chunk_off<D>(row, col);
-            cp_async_16(smem_u32(sK + so), srcK, bytes);  // bytes == 0: zero fill
-            cp_async_16(smem_u32(sV + so), srcV, bytes);
+        }
+#pragma unroll
+        for (int i = 0; i < kInsts; ++i) {
+            const int sl = __shfl_sync(0xffffffffu, slot, i * kRowsPerInst + my_sub);
+            const int row = (i * 4 + warp) * kRowsPerInst + my_sub;
+            const size_t off = sl >= 0 ? ((size_t)sl * p.hkv + kvh) * D + my_seg * 8 : 0;
+            const int bytes = sl >= 0 ? 16 : 0;  // 0: zero fill
+            const uint32_t so = chunk_off<D>(row, my_seg);
+            cp_async_16(smem_u32(sK + so), p.k_cache + off, bytes);
+            cp_async_16(smem_u32(sV + so), p.v_cache + off, bytes);
         }
     };
 
@@ -448,11 +462,14 @@ cudaError_t launch(const Args& a, const Plan& pl, float* part_o, float2* part_ml
     sp.hblocks = pl.hblocks;
     sp.group = a.group;
     sp.scale_log2 = a.scale * ATTN_LOG2E;
+    sp.page_shift = -1;
+    for (int sh = 0; sh < 31; ++sh)
+        if ((1 << sh) == a.page_size) sp.page_shift = sh;
     if (a.batch == 0) return cudaSuccess;
     cudaError_t e;
     if (a.head_dim == 64)
-        e = pl.nt == 1 ? launch_split<64, 1, 4>(sp, pl, a.batch, a.hkv, s)
-                       : launch_split<64, 2, 4>(sp, pl, a.batch, a.hkv, s);
+        e = pl.nt == 1 ? launch_split<64, 1, 3>(sp, pl, a.batch, a.hkv, s)
+                       : launch_split<64, 2, 3>(sp, pl, a.batch, a.hkv, s);
     else
         e = pl.nt == 1 ? launch_split<128, 1, 3>(sp, pl, a.batch, a.hkv, s)
                        : launch_split<128, 2, 3>(sp, pl, a.batch, a.hkv, s);
@@ -482,6 +499,7 @@ cudaError_t launch_visible_slots(const int32_t* seqlens, const int32_t* page_tab
     sp.seqlens = seqlens;
     sp.max_pages = max_pages;
     sp.page_size = page_size;
+    sp.page_shift = -1;
     sp.num_pages = num_pages;
     sp.win_first = win_first;
     sp.win_last = win_last;

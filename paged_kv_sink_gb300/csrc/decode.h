@@ -20,6 +20,7 @@ struct SplitParams {
     float2* part_ml;  // (batch, hq, max_splits): (running max in log2 units, sum)
     int max_pages, hq, hkv, page_size, num_pages, win_first, win_last;
     int split_tokens, max_splits, hblocks, group;
+    int page_shift;    // log2(page_size) when it is a power of two, else -1
     float scale_log2;  // softmax scale * log2(e)
 };
 
