@@ -9,18 +9,21 @@
 // first/last window of sglang PR "To implement attention-sink"), together with
 // LSE_i = m_i + ln(...) including the sink.
 //
-// One CTA = 128 query rows x (two query heads of one KV group, or one head
-// when the group size is odd); the two heads share every K/V tile.
-//   warp 0      TMA producer: Q once, then K/V tiles into a 3-stage ring
+// One CTA = 128 query rows of one query head; two CTAs share an SM, so the
+// tensor core interleaves two independent pipelines.
+//   warp 0      TMA producer: Q once, then the K tiles (3-stage ring)
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer:
-//               S_h = Q_h K^T (128x128, fp32 in TMEM), O_h += P_h V (128x64)
-//   warps 2,3   idle (complete warpgroup 0 for the register split)
-//   warps 4..11 two softmax warpgroups, one per head; thread = query row.
+//               S = Q K^T (128x128 fp32, A and B from shared memory),
+//               O += P V  (128x64 fp32, A = P from TMEM, B = V from shared memory)
+//   warp 2      TMA producer of the V tiles (2-stage ring: a V stage is needed
+//               only when the P V product is issued)
+//   warp 3      idle (completes warpgroup 0 for the register split)
+//   warps 4..7  softmax warpgroup; thread = query row.
+// TMEM (256 columns): S at 0, O at 128, P (bf16 pairs) at 192.
 // The online softmax starts from m = sink, l = 1 (the sink costs nothing per
 // tile).  The running reference max is only moved when a tile's max exceeds
 // it by more than 2^8 (then O in TMEM is rescaled in place), which keeps every
-// P value <= 256 and leaves the result exact.  P is written to shared memory
-// in the 128-byte-swizzled K-major layout the PV product reads.
+// P value <= 256 and leaves the result exact.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -35,26 +38,27 @@ using namespace sm103;
 constexpr int BM = 128;
 constexpr int BN = 128;
 constexpr int D = 64;
-constexpr int NSTAGE = 3;
-constexpr int kThreads = 384;
-// Register split (setmaxnreg): warpgroup 0 (TMA + MMA) gives registers to the
-// two softmax warpgroups.  128*56 + 256*224 = 64512 = 384 threads * 168, the
-// registers the block is launched with.
+constexpr int KSTAGE = 3;
+constexpr int VSTAGE = 2;
+constexpr int kThreads = 256;
+// Two CTAs per SM: 128 registers per thread at launch.  setmaxnreg moves them
+// from warpgroup 0 (TMA + MMA) to the softmax warpgroup:
+// 128*56 + 128*200 = 32768 = 256 threads * 128.
 constexpr int kRegsCtrl = 56;
-constexpr int kRegsSoftmax = 224;
+constexpr int kRegsSoftmax = 200;
 constexpr uint32_t kTile = 128 * 128;  // 128 rows x 128 bytes
-constexpr uint32_t kTmemCols = 512;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t cS = 0, cO = 128, cP = 192;  // TMEM columns
+constexpr float kRescaleThreshold = 8.0f;        // log2 units
 
 struct __align__(1024) Smem {
-    uint8_t q[2][kTile];
-    uint8_t k[NSTAGE][kTile];
-    uint8_t v[NSTAGE][kTile];
-    uint8_t p[2][2 * kTile];
+    uint8_t q[kTile];
+    uint8_t k[KSTAGE][kTile];
+    uint8_t v[VSTAGE][kTile];
     uint64_t q_full;
-    uint64_t kv_full[NSTAGE];
-    uint64_t kv_empty[NSTAGE];
-    uint64_t s_full[2], s_free[2], p_full[2], o_done[2];
+    uint64_t k_full[KSTAGE], k_empty[KSTAGE];
+    uint64_t v_full[VSTAGE], v_empty[VSTAGE];
+    uint64_t s_full, s_free, p_full, o_done;  // one phase per key tile
     uint64_t final_bar;
     uint32_t tmem_base;
     int abort;
@@ -66,7 +70,7 @@ struct Params {
     const int32_t* cu_k;
     __nv_bfloat16* out;
     float* lse;
-    int hq, group, nslot, n_rt, total_q, total_k;
+    int hq, group, n_rt, total_q, total_k;
     int win_first, win_last, causal;
     float scale_log2;
 };
@@ -78,14 +82,14 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     mbar_wait(bar, parity, &dummy);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int hu = blockIdx.x;
+    const int h = blockIdx.x;
     const int rt = p.n_rt - 1 - (int)blockIdx.y;  // heaviest row tiles first
     const int b = blockIdx.z;
 
@@ -94,16 +98,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int k_start = p.cu_k[b];
     int Lk = p.cu_k[b + 1] - k_start;
     if (q_start + Lq > p.total_q || k_start + Lk > p.total_k || Lq < 0 || Lk < 0) {
-        if (threadIdx.x == 0 && rt == 0 && hu == 0) raise_status(ATTN_SINK_DEV_SEQLEN_OOB);
+        if (threadIdx.x == 0 && rt == 0 && h == 0) raise_status(ATTN_SINK_DEV_SEQLEN_OOB);
         Lq = max(0, min(Lq, p.total_q - q_start));
         Lk = max(0, min(Lk, p.total_k - k_start));
     }
     const int qs = rt * BM;
     if (qs >= Lq) return;
-
-    const int nslot = p.nslot;
-    const int h0 = hu * nslot;
-    const int kvh = h0 / p.group;
+    const int kvh = h / p.group;
 
     // Tiles of keys visible to at least one valid row of this tile.
     const int off = Lk - Lq;
@@ -125,16 +126,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(&S.q_full, 1);
-        for (int s = 0; s < NSTAGE; ++s) {
-            mbar_init(&S.kv_full[s], 1);
-            mbar_init(&S.kv_empty[s], 1);
+        for (int s = 0; s < KSTAGE; ++s) {
+            mbar_init(&S.k_full[s], 1);
+            mbar_init(&S.k_empty[s], 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&S.s_full[s], 1);
-            mbar_init(&S.s_free[s], 128);
-            mbar_init(&S.p_full[s], 128);
-            mbar_init(&S.o_done[s], 1);
+        for (int s = 0; s < VSTAGE; ++s) {
+            mbar_init(&S.v_full[s], 1);
+            mbar_init(&S.v_empty[s], 1);
         }
+        mbar_init(&S.s_full, 1);
+        mbar_init(&S.s_free, 128);
+        mbar_init(&S.p_full, 128);
+        mbar_init(&S.o_done, 1);
         mbar_init(&S.final_bar, 1);
         S.abort = 0;
         fence_mbar_init();
@@ -150,164 +153,182 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort = &S.abort;
 
     if (warp < 4) {
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtrl));
-      if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            prefetch_tmap(&tm_q);
-            prefetch_tmap(&tm_k);
-            prefetch_tmap(&tm_v);
-            mbar_expect_tx(&S.q_full, nslot * kTile);
-            for (int s = 0; s < nslot; ++s) tma_load_3d(S.q[s], &tm_q, &S.q_full, 0, h0 + s, q_start + qs);
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtrl));
+        if ((warp == 0 || warp == 2) && lane == 0) {
+            // -------------------------------------------------------- producers
+            const bool is_k = warp == 0;
+            const int nst = is_k ? KSTAGE : VSTAGE;
+            uint64_t* full = is_k ? S.k_full : S.v_full;
+            uint64_t* empty = is_k ? S.k_empty : S.v_empty;
+            uint8_t* dst0 = is_k ? S.k[0] : S.v[0];
+            const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
+            prefetch_tmap(tm);
+            if (is_k) {
+                prefetch_tmap(&tm_q);
+                mbar_expect_tx(&S.q_full, kTile);
+                tma_load_3d(S.q, &tm_q, &S.q_full, 0, h, q_start + qs);
+            }
             int it = 0;
             for (; it < ntiles; ++it) {
-                const int st = it % NSTAGE;
-                if (it >= NSTAGE && !mbar_wait(&S.kv_empty[st], ((it / NSTAGE) - 1) & 1, abort)) break;
+                const int st = it % nst;
+                if (it >= nst && !mbar_wait(&empty[st], ((it / nst) - 1) & 1, abort)) break;
                 const int t = it < ta ? it : tb + (it - ta);
-                mbar_expect_tx(&S.kv_full[st], 2 * kTile);
-                tma_load_3d(S.k[st], &tm_k, &S.kv_full[st], 0, kvh, k_start + t * BN);
-                tma_load_3d(S.v[st], &tm_v, &S.kv_full[st], 0, kvh, k_start + t * BN);
+                mbar_expect_tx(&full[st], kTile);
+                tma_load_3d(dst0 + st * kTile, tm, &full[st], 0, kvh, k_start + t * BN);
             }
             // Drain: every copy issued must have landed before the CTA exits.
-            drain_wait(&S.q_full, 0);
-            for (int st = 0; st < NSTAGE; ++st) {
-                const int n = it > st ? (it - st + NSTAGE - 1) / NSTAGE : 0;
-                if (n > 0) drain_wait(&S.kv_full[st], (n - 1) & 1);
+            if (is_k) drain_wait(&S.q_full, 0);
+            for (int st = 0; st < nst; ++st) {
+                const int n = it > st ? (it - st + nst - 1) / nst : 0;
+                if (n > 0) drain_wait(&full[st], (n - 1) & 1);
             }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && ntiles > 0) {
+        } else if (warp == 1 && lane == 0 && ntiles > 0) {
+            // -------------------------------------------------------- MMA issuer
             constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false, false);
             constexpr uint32_t idO = idesc_bf16_f32(BM, D, false, true);
-            const uint32_t sq = smem_u32(S.q[0]), sk = smem_u32(S.k[0]), sv = smem_u32(S.v[0]);
-            const uint32_t sp = smem_u32(S.p[0]);
-            auto issue_S = [&](int it, int slot) {
-                const uint32_t kb = sk + (it % NSTAGE) * kTile;
-                const uint32_t qb = sq + slot * kTile;
+            const uint32_t sq = smem_u32(S.q), sk = smem_u32(S.k[0]), sv = smem_u32(S.v[0]);
+            auto issue_S = [&](int it) {
+                const uint32_t kb = sk + (it % KSTAGE) * kTile;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    umma_ss(tmem + slot * BN, sdesc_sw128(qb + kk * 32, 16, 1024), sdesc_sw128(kb + kk * 32, 16, 1024),
+                    umma_ss(tmem + cS, sdesc_sw128(sq + kk * 32, 16, 1024), sdesc_sw128(kb + kk * 32, 16, 1024),
                             idS, kk > 0);
-                umma_commit(&S.s_full[slot]);
+                umma_commit(&S.s_full);
+                umma_commit(&S.k_empty[it % KSTAGE]);
             };
-            auto issue_PV = [&](int it, int slot) {
-                const uint32_t vb = sv + (it % NSTAGE) * kTile;
-                const uint32_t pb = sp + slot * 2 * kTile;
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    umma_ss(tmem + 2 * BN + slot * D,
-                            sdesc_sw128(pb + (kk >> 2) * kTile + (kk & 3) * 32, 16, 1024),
-                            sdesc_sw128(vb + kk * 2048, 8192, 1024), idO, (it > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(&S.o_done[slot]);
-            };
-            bool ok = mbar_wait(&S.q_full, 0, abort) && mbar_wait(&S.kv_full[0], 0, abort);
+            bool ok = mbar_wait(&S.q_full, 0, abort) && mbar_wait(&S.k_full[0], 0, abort);
             if (ok) {
                 tc_fence_after();
-                for (int s = 0; s < nslot; ++s) issue_S(0, s);
+                issue_S(0);
             }
             for (int it = 0; ok && it < ntiles; ++it) {
                 const int nx = it + 1;
-                // Both heads' next S as soon as their softmax has read this S
-                // (it runs on the tensor core while the softmax works) ...
+                // The next S as soon as the softmax has read this one (it runs on
+                // the tensor core while the softmax works) ...
                 if (nx < ntiles) {
-                    if (!(ok = mbar_wait(&S.kv_full[nx % NSTAGE], (nx / NSTAGE) & 1, abort))) break;
-                    for (int s = 0; s < nslot && ok; ++s) {
-                        if (!(ok = mbar_wait(&S.s_free[s], it & 1, abort))) break;
-                        tc_fence_after();
-                        issue_S(nx, s);
-                    }
-                    if (!ok) break;
-                }
-                // ... then each head's P V once its P is in shared memory.
-                for (int s = 0; s < nslot && ok; ++s) {
-                    if (!(ok = mbar_wait(&S.p_full[s], it & 1, abort))) break;
+                    if (!(ok = mbar_wait(&S.k_full[nx % KSTAGE], (nx / KSTAGE) & 1, abort))) break;
+                    if (!(ok = mbar_wait(&S.s_free, it & 1, abort))) break;
                     tc_fence_after();
-                    issue_PV(it, s);
+                    issue_S(nx);
                 }
-                if (ok) umma_commit(&S.kv_empty[it % NSTAGE]);
+                // ... then O += P V once P is in TMEM (8 columns of bf16 pairs per 16 keys).
+                if (!(ok = mbar_wait(&S.v_full[it % VSTAGE], (it / VSTAGE) & 1, abort))) break;
+                if (!(ok = mbar_wait(&S.p_full, it & 1, abort))) break;
+                tc_fence_after();
+                const uint32_t vb = sv + (it % VSTAGE) * kTile;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    umma_ts(tmem + cO, tmem + cP + kk * 8, sdesc_sw128(vb + kk * 2048, 8192, 1024), idO,
+                            (it > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(&S.o_done);
+                umma_commit(&S.v_empty[it % VSTAGE]);
             }
             // Every MMA issued must be complete before TMEM is released.
             umma_commit(&S.final_bar);
             drain_wait(&S.final_bar, 0);
         }
-      }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
         // ------------------------------------------------------------ softmax
-        const int slot = (warp - 4) >> 2;
-        if (slot < nslot) {
-            const int q4 = warp & 3;
-            const int r = q4 * 32 + lane;
-            const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
-            const uint32_t tS = tmem + lane_base + slot * BN;
-            const uint32_t tO = tmem + lane_base + 2 * BN + slot * D;
-            const int h = h0 + slot;
-            const float sg = p.sink ? p.sink[h] * ATTN_LOG2E : -INFINITY;
-            const float sl2 = p.scale_log2;
-            float m_ref = sg;
-            float l = sg == -INFINITY ? 0.f : 1.f;
-            const int pos = off + qs + r;
-            uint8_t* prow = S.p[slot];
-            bool ok = true;
-            for (int it = 0; it < ntiles; ++it) {
-                const int t = it < ta ? it : tb + (it - ta);
-                const int j0 = t * BN;
-                ok = mbar_wait(&S.s_full[slot], it & 1, abort);
+        const int q4 = warp & 3;
+        const int r = q4 * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+        const uint32_t tS = tmem + lane_base + cS;
+        const uint32_t tO = tmem + lane_base + cO;
+        const uint32_t tP = tmem + lane_base + cP;
+        const float sg = p.sink ? p.sink[h] * ATTN_LOG2E : -INFINITY;
+        const float sl2 = p.scale_log2;
+        float m_ref = sg;
+        float l = sg == -INFINITY ? 0.f : 1.f;
+        const int pos = off + qs + r;
+        bool ok = true;
+        for (int it = 0; it < ntiles; ++it) {
+            const int t = it < ta ? it : tb + (it - ta);
+            const int j0 = t * BN;
+            ok = mbar_wait(&S.s_full, it & 1, abort);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t s[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(&S.s_free);
+
+            const int jmax = j0 + BN - 1;
+            const bool full = (!p.causal || jmax <= P0) && (jmax < Lk) &&
+                              (p.win_last <= 0 || jmax < p.win_first || j0 >= P1 + 1 - p.win_last);
+            if (!full) {
+                int c_hi = p.causal ? pos - j0 + 1 : BN;
+                c_hi = min(c_hi, Lk - j0);
+                const int f_hi = p.win_last > 0 ? p.win_first - j0 : BN;
+                const int w_lo = p.win_last > 0 ? pos + 1 - p.win_last - j0 : 0;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int cc = c * 32 + i;
+                        const bool vis = cc < c_hi && (cc < f_hi || cc >= w_lo);
+                        if (!vis) s[c][i] = __float_as_uint(-INFINITY);
+                    }
+            }
+            // Row max: eight independent 3-input max chains of 16 values.
+            float mc[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t* v = &s[k >> 1][(k & 1) * 16];
+                float m = max3f(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+#pragma unroll
+                for (int i = 3; i < 15; i += 2) m = max3f(m, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+                mc[k] = fmaxf(m, __uint_as_float(v[15]));
+            }
+            const float mx = max3f(max3f(mc[0], mc[1], mc[2]), max3f(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
+            const float m_new = fmaxf(m_ref, mx * sl2);
+            const bool resc = m_new > m_ref + kRescaleThreshold;
+            const float alpha = resc ? fast_exp2(m_ref - m_new) : 1.f;
+            if (resc) {
+                l *= alpha;
+                m_ref = m_new;
+            }
+            const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+            // P = 2^(s*scale*log2e - m) into registers (packed fp32x2 FMA, MUFU ex2,
+            // packed partial sums) before waiting for the previous P V.
+            const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(-m_use, -m_use);
+            uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+            uint32_t w[64];
+#pragma unroll
+            for (int e = 0; e < 64; ++e) {
+                const int i0 = 2 * e;
+                const uint64_t y = f2_fma(f2_pack(__uint_as_float(s[i0 >> 5][i0 & 31]),
+                                                  __uint_as_float(s[(i0 + 1) >> 5][(i0 + 1) & 31])),
+                                          sc2, nm2);
+                float y0, y1;
+                f2_unpack(y, y0, y1);
+                const float x0 = fast_exp2(y0), x1 = fast_exp2(y1);
+                acc2[e & 3] = f2_add(acc2[e & 3], f2_pack(x0, x1));
+                w[e] = pack_bf16x2(x0, x1);
+            }
+            float rs = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float lo, hi;
+                f2_unpack(acc2[e], lo, hi);
+                rs += lo + hi;
+            }
+            l += rs;
+            if (it > 0) {
+                // The previous P V must be complete: it reads P in TMEM and
+                // accumulates into the O that a rescale touches.
+                ok = mbar_wait(&S.o_done, (it - 1) & 1, abort);
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                uint32_t s[4][32];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
-                tmem_ld_wait();
-                tc_fence_before();
-                mbar_arrive(&S.s_free[slot]);
-
-                const int jmax = j0 + BN - 1;
-                const bool full = (!p.causal || jmax <= P0) && (jmax < Lk) &&
-                                  (p.win_last <= 0 || jmax < p.win_first || j0 >= P1 + 1 - p.win_last);
-                if (!full) {
-                    int c_hi = p.causal ? pos - j0 + 1 : BN;
-                    c_hi = min(c_hi, Lk - j0);
-                    const int f_hi = p.win_last > 0 ? p.win_first - j0 : BN;
-                    const int w_lo = p.win_last > 0 ? pos + 1 - p.win_last - j0 : 0;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const int cc = c * 32 + i;
-                            const bool vis = cc < c_hi && (cc < f_hi || cc >= w_lo);
-                            if (!vis) s[c][i] = __float_as_uint(-INFINITY);
-                        }
-                }
-                // Row max: eight independent 3-input max chains of 16 values.
-                float mc[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t* v = &s[k >> 1][(k & 1) * 16];
-                    float m = max3f(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
-#pragma unroll
-                    for (int i = 3; i < 15; i += 2) m = max3f(m, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
-                    mc[k] = fmaxf(m, __uint_as_float(v[15]));
-                }
-                const float mx =
-                    max3f(max3f(mc[0], mc[1], mc[2]), max3f(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
-                const float m_new = fmaxf(m_ref, mx * sl2);
-                const bool resc = m_new > m_ref + kRescaleThreshold;
-                const float alpha = resc ? fast_exp2(m_ref - m_new) : 1.f;
-                bool waited = false;
-                if (it > 0 && __any_sync(0xffffffffu, resc)) {
-                    // O holds PV of earlier tiles: wait for the last one, then rescale in TMEM.
-                    ok = mbar_wait(&S.o_done[slot], (it - 1) & 1, abort);
-                    if (!__all_sync(0xffffffffu, ok)) {
-                        ok = false;
-                        break;
-                    }
-                    waited = true;
-                    tc_fence_after();
+                if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         uint32_t o[32];
@@ -317,90 +338,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
                         tmem_st32(tO + half * 32, o);
                     }
-                    tmem_st_wait();
-                }
-                if (resc) {
-                    l *= alpha;
-                    m_ref = m_new;
-                }
-                const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-                if (it > 0 && !waited) {
-                    // the previous PV must be done reading this head's P buffer
-                    ok = mbar_wait(&S.o_done[slot], (it - 1) & 1, abort);
-                    if (!__all_sync(0xffffffffu, ok)) {
-                        ok = false;
-                        break;
-                    }
-                }
-                // P = 2^(s*scale*log2e - m): packed fp32x2 FMA, MUFU ex2, packed partial sums.
-                const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(-m_use, -m_use);
-                uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-                for (int cc = 0; cc < 16; ++cc) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int i0 = cc * 8 + 2 * e;
-                        const uint64_t y = f2_fma(f2_pack(__uint_as_float(s[i0 >> 5][i0 & 31]),
-                                                          __uint_as_float(s[(i0 + 1) >> 5][(i0 + 1) & 31])),
-                                                  sc2, nm2);
-                        float y0, y1;
-                        f2_unpack(y, y0, y1);
-                        const float x0 = fast_exp2(y0), x1 = fast_exp2(y1);
-                        acc2[e] = f2_add(acc2[e], f2_pack(x0, x1));
-                        w[e] = pack_bf16x2(x0, x1);
-                    }
-                    uint8_t* dst = prow + (cc >> 3) * kTile + sw128_off(r, cc & 7);
-                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(smem_u32(dst)), "r"(w[0]),
-                                 "r"(w[1]), "r"(w[2]), "r"(w[3])
-                                 : "memory");
-                }
-                float rs = 0.f;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float lo, hi;
-                    f2_unpack(acc2[e], lo, hi);
-                    rs += lo + hi;
-                }
-                l += rs;
-                fence_proxy_async_smem();
-                tc_fence_before();
-                mbar_arrive(&S.p_full[slot]);
-            }
-
-            // ---------------------------------------------------------- epilogue
-            if (ok && ntiles > 0) ok = mbar_wait(&S.o_done[slot], (ntiles - 1) & 1, abort);
-            ok = __all_sync(0xffffffffu, ok);
-            const bool have = ok && ntiles > 0;
-            if (have) tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            const int row = q_start + qs + r;
-            const bool store = r < rows_valid && ok;
-            uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)row * p.hq + h) * D);
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t u[32];
-                if (have) {  // warp-uniform: every lane takes part in the collective load
-                    tmem_ld32(tO + half * 32, u);
-                    tmem_ld_wait();
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) u[i] = 0u;
-                }
-                if (store) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(u[8 * c + 0]) * inv, __uint_as_float(u[8 * c + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(u[8 * c + 2]) * inv, __uint_as_float(u[8 * c + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(u[8 * c + 4]) * inv, __uint_as_float(u[8 * c + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(u[8 * c + 6]) * inv, __uint_as_float(u[8 * c + 7]) * inv);
-                        dst[half * 4 + c] = w;
-                    }
                 }
             }
-            if (store && p.lse) p.lse[(size_t)h * p.total_q + row] = l > 0.f ? (m_ref + log2f(l)) * ATTN_LN2 : -INFINITY;
+            // P as bf16 pairs: TMEM column c holds keys 2c (low half) and 2c+1.
+            tmem_st32(tP, *reinterpret_cast<uint32_t(*)[32]>(&w[0]));
+            tmem_st32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&w[32]));
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&S.p_full);
         }
+
+        // -------------------------------------------------------------- epilogue
+        if (ok && ntiles > 0) ok = mbar_wait(&S.o_done, (ntiles - 1) & 1, abort);
+        ok = __all_sync(0xffffffffu, ok);
+        const bool have = ok && ntiles > 0;
+        if (have) tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const int row = q_start + qs + r;
+        const bool store = r < rows_valid && ok;
+        uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)row * p.hq + h) * D);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            uint32_t u[32];
+            if (have) {  // warp-uniform: every lane takes part in the collective load
+                tmem_ld32(tO + half * 32, u);
+                tmem_ld_wait();
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) u[i] = 0u;
+            }
+            if (store) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint4 wv;
+                    wv.x = pack_bf16x2(__uint_as_float(u[8 * c + 0]) * inv, __uint_as_float(u[8 * c + 1]) * inv);
+                    wv.y = pack_bf16x2(__uint_as_float(u[8 * c + 2]) * inv, __uint_as_float(u[8 * c + 3]) * inv);
+                    wv.z = pack_bf16x2(__uint_as_float(u[8 * c + 4]) * inv, __uint_as_float(u[8 * c + 5]) * inv);
+                    wv.w = pack_bf16x2(__uint_as_float(u[8 * c + 6]) * inv, __uint_as_float(u[8 * c + 7]) * inv);
+                    dst[half * 4 + c] = wv;
+                }
+            }
+        }
+        if (store && p.lse) p.lse[(size_t)h * p.total_q + row] = l > 0.f ? (m_ref + log2f(l)) * ATTN_LN2 : -INFINITY;
     }
 
     tc_fence_before();
@@ -464,7 +443,6 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s, std::string* what) {
     p.lse = a.lse;
     p.hq = a.hq;
     p.group = a.hq / a.hkv;
-    p.nslot = (p.group % 2 == 0) ? 2 : 1;
     p.n_rt = (a.max_seqlen_q + BM - 1) / BM;
     p.total_q = a.total_q;
     p.total_k = a.total_k;
@@ -478,7 +456,7 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s, std::string* what) {
         *what = "smem attribute";
         return e;
     }
-    dim3 grid(a.hq / p.nslot, p.n_rt, a.batch);
+    dim3 grid(a.hq, p.n_rt, a.batch);
     fwd_kernel<<<grid, kThreads, smem, s>>>(tq, tk, tv, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) *what = "launch";

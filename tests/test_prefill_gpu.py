@@ -48,6 +48,8 @@ CASES = {
     "sliding_only": ([300], [600], 2, 2, "normal", 0, 64, True),
     "more_q_than_k": ([300, 10], [100, 0], 4, 2, "normal", 0, 0, True),
     "group8_long": ([1000], [3000], 16, 2, (-2.0, 4.0), 0, 0, True),
+    # many key tiles per CTA: the softmax can run ahead of the MMA issuer
+    "long_prefix": ([256, 384], [20000, 16384], 4, 2, (-2.0, 4.0), 0, 0, True),
 }
 
 
