@@ -20,7 +20,7 @@
 //    128 query columns).  They write P^T and dS^T to shared memory in the
 //    128-byte-swizzled layout (dS^T is read K-major for dK and MN-major, as dS,
 //    for dQ), and add the previous step's dQ tile (TMEM, double-buffered) to an
-//    fp32 accumulator with 16-byte vector atomics.  dK/dV are summed over the
+//    fp32 accumulator with TMA bulk tensor reduce-adds.  dK/dV are summed over the
 //    group in TMEM (no atomics).
 //  * bwd_dq_convert_kernel: fp32 dQ accumulator -> bf16.
 #include <cudaTypedefs.h>
@@ -53,6 +53,7 @@ struct __align__(1024) Smem {
     uint8_t dout[2][kTile];
     uint8_t pt[2 * kTile];   // P^T  (128 keys x 128 queries), two 64-query atoms
     uint8_t dst[2 * kTile];  // dS^T (same layout)
+    uint8_t dq_stage[2][kTile];  // dQ tile staging: two 32-column fp32 halves, 128-byte swizzled rows
     float nlse2[2][BM];      // -LSE * log2(e) of the current query tile (-inf for rows past the end)
     float nd[2][BM];         // -D of the current query tile (0 past the end)
     uint64_t kv_full;
@@ -60,7 +61,10 @@ struct __align__(1024) Smem {
     uint64_t sdp_full, sdp_free, pds_full, mma2_done;  // per step
     uint64_t dq_free[2];
     uint64_t lse_ready[2];  // the elementwise warps have filled nlse2/nd[buf]
-    uint64_t final_bar;
+    uint64_t dq_staged;     // all elementwise threads wrote their part of the dQ tile
+    uint64_t dq_stage_free; // the bulk reduce has finished reading the staging buffer
+    uint64_t final_bar;  // dV / dK / dQ issuer done
+    uint64_t final_sdp;  // S^T / dP^T issuer done
     uint32_t tmem_base;
     int abort;
 };
@@ -81,11 +85,6 @@ struct MainParams {
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     int dummy = 0;
     mbar_wait(bar, parity, &dummy);
-}
-
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
 }
 
 // Query tiles of one head that see at least one key of [j0, j0 + BN).
@@ -115,7 +114,7 @@ __device__ __forceinline__ QRange query_tiles(int j0, int Lq, int Lk, int causal
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const MainParams p) {
+                    const __grid_constant__ CUtensorMap tm_dq, const MainParams p) {
     extern __shared__ uint8_t smem_raw[];
     Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -149,7 +148,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&S.sdp_free, kWork);
         mbar_init(&S.pds_full, kWork);
         mbar_init(&S.mma2_done, 1);
+        mbar_init(&S.dq_staged, kWork);
+        mbar_init(&S.dq_stage_free, 1);
         mbar_init(&S.final_bar, 1);
+        mbar_init(&S.final_sdp, 1);
         S.abort = 0;
         fence_mbar_init();
     }
@@ -189,62 +191,64 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int n = t > st ? (t - st + 1) / 2 : 0;
                 if (n > 0) drain_wait(&S.qdo_full[st], (n - 1) & 1);
             }
-        } else if (warp == 1 && lane == 0 && T > 0) {
-            // -------------------------------------------------------- MMA issuer
+        } else if ((warp == 1 || warp == 3) && lane == 0 && T > 0) {
+            // -------------------------------------------------------- MMA issuers
+            // Two issue threads feed the tensor core independent instruction
+            // streams: warp 1 issues each step's S^T / dP^T as soon as the
+            // elementwise warps have read the previous ones; warp 3 issues the
+            // step's dV / dK / dQ once P^T and dS^T are in shared memory.
+            // Within each stream the independent accumulator chains are
+            // interleaved k-step by k-step.
             constexpr uint32_t idSS = idesc_bf16_f32(BN, BM, false, false);  // S^T, dP^T
             constexpr uint32_t idKN = idesc_bf16_f32(BN, D, false, true);    // dV, dK: A K-major, B MN-major
             constexpr uint32_t idQ = idesc_bf16_f32(BM, D, true, true);      // dQ: A (dS) MN-major, B (K) MN-major
             const uint32_t sk = smem_u32(S.k), sv = smem_u32(S.v);
             const uint32_t spt = smem_u32(S.pt), sds = smem_u32(S.dst);
-            auto issue_sdp = [&](int t) {
-                const uint32_t sq = smem_u32(S.q[t & 1]), sdo = smem_u32(S.dout[t & 1]);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    umma_ss(tmem + cS, sdesc_sw128(sk + kk * 32, 16, 1024), sdesc_sw128(sq + kk * 32, 16, 1024),
-                            idSS, kk > 0);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    umma_ss(tmem + cDP, sdesc_sw128(sv + kk * 32, 16, 1024),
-                            sdesc_sw128(sdo + kk * 32, 16, 1024), idSS, kk > 0);
-                umma_commit(&S.sdp_full);
-            };
-            bool ok = mbar_wait(&S.kv_full, 0, abort) && mbar_wait(&S.qdo_full[0], 0, abort);
-            if (ok) {
-                tc_fence_after();
-                issue_sdp(0);
-            }
-            for (int t = 0; ok && t < T; ++t) {
-                const int st = t & 1;
-                if (t + 1 < T) {
-                    // next step's S^T / dP^T as soon as the softmax has read this step's
-                    if (!(ok = mbar_wait(&S.qdo_full[(t + 1) & 1], ((t + 1) >> 1) & 1, abort))) break;
-                    if (!(ok = mbar_wait(&S.sdp_free, t & 1, abort))) break;
+            bool ok = mbar_wait(&S.kv_full, 0, abort);
+            if (warp == 1) {
+                for (int t = 0; ok && t < T; ++t) {
+                    if (!(ok = mbar_wait(&S.qdo_full[t & 1], (t >> 1) & 1, abort))) break;
+                    if (t > 0 && !(ok = mbar_wait(&S.sdp_free, (t - 1) & 1, abort))) break;
                     tc_fence_after();
-                    issue_sdp(t + 1);
-                }
-                if (!(ok = mbar_wait(&S.pds_full, t & 1, abort))) break;
-                if (t >= 2 && !(ok = mbar_wait(&S.dq_free[st], ((t >> 1) - 1) & 1, abort))) break;
-                tc_fence_after();
-                const uint32_t sq = smem_u32(S.q[st]), sdo = smem_u32(S.dout[st]);
+                    const uint32_t sq = smem_u32(S.q[t & 1]), sdo = smem_u32(S.dout[t & 1]);
 #pragma unroll
-                for (int kk = 0; kk < BM / 16; ++kk) {
-                    const uint32_t koff = (kk >> 2) * kTile + (kk & 3) * 32;  // K-major step over queries
-                    const uint32_t moff = kk * 2048;                          // MN-major step over K rows
-                    const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
-                    umma_ss(tmem + cDV, sdesc_sw128(spt + koff, 16, 1024), sdesc_sw128(sdo + moff, 8192, 1024),
-                            idKN, acc);
-                    umma_ss(tmem + cDK, sdesc_sw128(sds + koff, 16, 1024), sdesc_sw128(sq + moff, 8192, 1024),
-                            idKN, acc);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        umma_ss(tmem + cS, sdesc_sw128(sk + kk * 32, 16, 1024), sdesc_sw128(sq + kk * 32, 16, 1024),
+                                idSS, kk > 0);
+                        umma_ss(tmem + cDP, sdesc_sw128(sv + kk * 32, 16, 1024),
+                                sdesc_sw128(sdo + kk * 32, 16, 1024), idSS, kk > 0);
+                    }
+                    umma_commit(&S.sdp_full);
                 }
+                // Every MMA this thread issued must be complete before TMEM is released.
+                umma_commit(&S.final_sdp);
+                drain_wait(&S.final_sdp, 0);
+            } else {
+                for (int t = 0; ok && t < T; ++t) {
+                    const int st = t & 1;
+                    if (!(ok = mbar_wait(&S.pds_full, t & 1, abort))) break;
+                    if (t >= 2 && !(ok = mbar_wait(&S.dq_free[st], ((t >> 1) - 1) & 1, abort))) break;
+                    tc_fence_after();
+                    const uint32_t sq = smem_u32(S.q[st]), sdo = smem_u32(S.dout[st]);
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    umma_ss(tmem + cDQ + st * D, sdesc_sw128(sds + kk * 2048, kTile, 1024),
-                            sdesc_sw128(sk + kk * 2048, 8192, 1024), idQ, kk > 0);
-                umma_commit(&S.mma2_done);
-                umma_commit(&S.qdo_empty[st]);
+                    for (int kk = 0; kk < BM / 16; ++kk) {
+                        const uint32_t koff = (kk >> 2) * kTile + (kk & 3) * 32;  // K-major step over queries
+                        const uint32_t moff = kk * 2048;                          // MN-major step over K rows
+                        const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
+                        umma_ss(tmem + cDV, sdesc_sw128(spt + koff, 16, 1024), sdesc_sw128(sdo + moff, 8192, 1024),
+                                idKN, acc);
+                        umma_ss(tmem + cDK, sdesc_sw128(sds + koff, 16, 1024), sdesc_sw128(sq + moff, 8192, 1024),
+                                idKN, acc);
+                        // dQ k-step kk runs over keys 16 kk .. 16 kk + 15 (BN == BM)
+                        umma_ss(tmem + cDQ + st * D, sdesc_sw128(sds + kk * 2048, kTile, 1024),
+                                sdesc_sw128(sk + kk * 2048, 8192, 1024), idQ, kk > 0);
+                    }
+                    umma_commit(&S.mma2_done);
+                    umma_commit(&S.qdo_empty[st]);
+                }
+                umma_commit(&S.final_bar);
+                drain_wait(&S.final_bar, 0);
             }
-            umma_commit(&S.final_bar);
-            drain_wait(&S.final_bar, 0);
         }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsWork));
@@ -258,8 +262,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
         bool ok = true;
 
-        // dQ of step tt (its GEMMs are complete): 32 columns of this lane's query row.
-        auto flush_dq = [&](int tt) {
+        // dQ of step tt (its GEMMs are complete): this lane's query row, 32 columns
+        // (half ch), staged in shared memory and added to the fp32 accumulator by
+        // two TMA bulk reduce-adds issued by one thread.
+        auto flush_dq = [&](int tt) -> bool {
             const int hh = kvh * p.group + tt / nqt;
             const int qq0 = (qr.lo + tt % nqt) * BM;
             uint32_t u[32];
@@ -267,14 +273,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(&S.dq_free[tt & 1]);
-            if (qq0 + j < Lq) {
-                float* dst = p.dq_accum + ((size_t)(q_start + qq0 + j) * p.hq + hh) * D + ch * 32;
-                const float f = p.scale;
+            bool fine = tt == 0 || mbar_wait(&S.dq_stage_free, (tt - 1) & 1, abort);
+            if (!__all_sync(0xffffffffu, fine)) return false;
+            const float f = qq0 + j < Lq ? p.scale : 0.f;  // rows past the request add zero
+            uint8_t* stage = S.dq_stage[ch];
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    red_add_v4(dst + 4 * c, __uint_as_float(u[4 * c]) * f, __uint_as_float(u[4 * c + 1]) * f,
-                               __uint_as_float(u[4 * c + 2]) * f, __uint_as_float(u[4 * c + 3]) * f);
+            for (int c = 0; c < 8; ++c) {
+                asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(smem_u32(stage + sw128_off(j, c))),
+                             "f"(__uint_as_float(u[4 * c]) * f), "f"(__uint_as_float(u[4 * c + 1]) * f),
+                             "f"(__uint_as_float(u[4 * c + 2]) * f), "f"(__uint_as_float(u[4 * c + 3]) * f)
+                             : "memory");
             }
+            fence_proxy_async_smem();
+            mbar_arrive(&S.dq_staged);
+            if (tid == 0) {
+                if (!mbar_wait(&S.dq_staged, tt & 1, abort)) return false;
+                tma_reduce_add_3d(&tm_dq, S.dq_stage[0], 0, hh, q_start + qq0);
+                tma_reduce_add_3d(&tm_dq, S.dq_stage[1], 32, hh, q_start + qq0);
+                bulk_commit_group();
+                bulk_wait_read_all();
+                mbar_arrive(&S.dq_stage_free);
+            }
+            return true;
         };
 
         for (int t = 0; t < T; ++t) {
@@ -363,7 +383,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&S.pds_full);
             if (t > 0) {
                 tc_fence_after();
-                flush_dq(t - 1);
+                if (!__all_sync(0xffffffffu, flush_dq(t - 1))) {
+                    ok = false;
+                    break;
+                }
             }
         }
         // last step's dQ, then dK (column half 0) / dV (column half 1)
@@ -372,13 +395,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
                 tc_fence_after();
-                flush_dq(T - 1);
+                ok = __all_sync(0xffffffffu, flush_dq(T - 1));
             }
         }
         if (ok && T > 0) ok = mbar_wait(&S.final_bar, 0, abort);
         ok = __all_sync(0xffffffffu, ok);
         const bool have = ok && T > 0;
         if (have) tc_fence_after();
+        if (tid == 0) bulk_wait_all();  // the dQ reduce-adds have landed
         const size_t rowoff = ((size_t)(k_start + kpos) * p.hkv + kvh) * D;
         const uint32_t col = ch == 0 ? cDK : cDV;
         const float f = ch == 0 ? p.scale : 1.f;
@@ -483,6 +507,7 @@ __global__ void bwd_dq_convert_kernel(const float4* __restrict__ acc, uint2* __r
 // Host side
 
 cudaError_t make_map(CUtensorMap* m, const void* base, int heads, long long rows, std::string* what);
+cudaError_t make_map_dq(CUtensorMap* m, const float* base, int heads, long long rows, std::string* what);
 
 size_t workspace_bytes(const Args& a) {
     const size_t acc = (size_t)a.total_q * a.hq * D * sizeof(float);
@@ -523,6 +548,27 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int heads, long long rows
     return cudaSuccess;
 }
 
+// (rows, heads, 64) fp32 dQ accumulator as {d, head, row}; box {32, 1, 128}, 128-byte swizzle.
+cudaError_t make_map_dq(CUtensorMap* m, const float* base, int heads, long long rows, std::string* what) {
+    auto fn = encode_fn();
+    if (!fn) {
+        *what = "cuTensorMapEncodeTiled unavailable";
+        return cudaErrorNotSupported;
+    }
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1)};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)D * 4 * heads};
+    cuuint32_t box[3] = {32, 1, 128};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        *what = "cuTensorMapEncodeTiled (dQ) failed (" + std::to_string((int)r) + ")";
+        return cudaErrorInvalidValue;
+    }
+    return cudaSuccess;
+}
+
 cudaError_t launch(const Args& a, void* workspace, size_t ws_bytes, cudaStream_t s, std::string* what) {
     if (a.total_q == 0 && a.total_k == 0) return cudaSuccess;
     cudaError_t e;
@@ -554,11 +600,12 @@ cudaError_t launch(const Args& a, void* workspace, size_t ws_bytes, cudaStream_t
         }
     }
     if (a.total_q > 0 && a.total_k > 0 && a.max_seqlen_k > 0) {
-        CUtensorMap tq, tk, tv, tdo;
+        CUtensorMap tq, tk, tv, tdo, tdq;
         if ((e = make_map(&tq, a.q, a.hq, a.total_q, what)) != cudaSuccess) return e;
         if ((e = make_map(&tk, a.k, a.hkv, a.total_k, what)) != cudaSuccess) return e;
         if ((e = make_map(&tv, a.v, a.hkv, a.total_k, what)) != cudaSuccess) return e;
         if ((e = make_map(&tdo, a.dout, a.hq, a.total_q, what)) != cudaSuccess) return e;
+        if ((e = make_map_dq(&tdq, dq_accum, a.hq, a.total_q, what)) != cudaSuccess) return e;
         MainParams p;
         p.cu_q = a.cu_q;
         p.cu_k = a.cu_k;
@@ -584,7 +631,7 @@ cudaError_t launch(const Args& a, void* workspace, size_t ws_bytes, cudaStream_t
             return e;
         }
         dim3 g2((a.max_seqlen_k + BN - 1) / BN, a.hkv, a.batch);
-        bwd_main_kernel<<<g2, kThreads, smem, s>>>(tq, tk, tv, tdo, p);
+        bwd_main_kernel<<<g2, kThreads, smem, s>>>(tq, tk, tv, tdo, tdq, p);
         if ((e = cudaGetLastError()) != cudaSuccess) {
             *what = "main launch";
             return e;
