@@ -118,7 +118,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kt = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    // Grid (KV head, request, key tile) with the key tile slowest: causal key
+    // tile 0 is seen by every query tile, so launching tiles in increasing order
+    // starts the longest CTAs first and leaves short ones for the tail.
+    const int kvh = blockIdx.x, b = blockIdx.y, kt = blockIdx.z;
 
     const int q_start = p.cu_q[b];
     int Lq = p.cu_q[b + 1] - q_start;
@@ -630,7 +633,7 @@ cudaError_t launch(const Args& a, void* workspace, size_t ws_bytes, cudaStream_t
             *what = "smem attribute";
             return e;
         }
-        dim3 g2((a.max_seqlen_k + BN - 1) / BN, a.hkv, a.batch);
+        dim3 g2(a.hkv, a.batch, (a.max_seqlen_k + BN - 1) / BN);
         bwd_main_kernel<<<g2, kThreads, smem, s>>>(tq, tk, tv, tdo, tdq, p);
         if ((e = cudaGetLastError()) != cudaSuccess) {
             *what = "main launch";
