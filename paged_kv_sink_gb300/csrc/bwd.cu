@@ -38,8 +38,8 @@ constexpr int BM = 128;  // query rows per tile
 constexpr int BN = 128;  // keys per CTA
 constexpr int D = 64;
 constexpr int kThreads = 384;
-constexpr int kRegsCtrl = 88;
-constexpr int kRegsWork = 208;  // 128*88 + 256*208 = 64512 = 384 * 168
+constexpr int kRegsCtrl = 104;
+constexpr int kRegsWork = 200;  // 128*104 + 256*200 = 64512 = 384 * 168
 constexpr int kWork = 256;      // elementwise threads: warps 4..11
 constexpr uint32_t kTile = 128 * 128;
 constexpr uint32_t kTmemCols = 512;
@@ -194,6 +194,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int n = t > st ? (t - st + 1) / 2 : 0;
                 if (n > 0) drain_wait(&S.qdo_full[st], (n - 1) & 1);
             }
+        } else if (warp == 2 && lane == 0 && T > 0) {
+            // -------------------------------------------------------- dQ reducer
+            // Adds each staged dQ tile (two 32-column fp32 halves) to the fp32
+            // accumulator with TMA bulk tensor reduce-adds, then frees the stage.
+            for (int tt = 0; tt < T; ++tt) {
+                if (!mbar_wait(&S.dq_staged, tt & 1, abort)) break;
+                const int hh = kvh * p.group + tt / nqt;
+                const int qq0 = (qr.lo + tt % nqt) * BM;
+                tma_reduce_add_3d(&tm_dq, S.dq_stage[0], 0, hh, q_start + qq0);
+                tma_reduce_add_3d(&tm_dq, S.dq_stage[1], 32, hh, q_start + qq0);
+                bulk_commit_group();
+                bulk_wait_read_all();
+                mbar_arrive(&S.dq_stage_free);
+            }
+            bulk_wait_all();  // the reduce-adds have landed before the CTA exits
         } else if ((warp == 1 || warp == 3) && lane == 0 && T > 0) {
             // -------------------------------------------------------- MMA issuers
             // Two issue threads feed the tensor core independent instruction
@@ -266,8 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
 
         // dQ of step tt (its GEMMs are complete): this lane's query row, 32 columns
-        // (half ch), staged in shared memory and added to the fp32 accumulator by
-        // two TMA bulk reduce-adds issued by one thread.
+        // (half ch), staged in shared memory; warp 2 adds the tile to the fp32
+        // accumulator with TMA bulk reduce-adds.
         auto flush_dq = [&](int tt) -> bool {
             const int hh = kvh * p.group + tt / nqt;
             const int qq0 = (qr.lo + tt % nqt) * BM;
@@ -288,15 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                              : "memory");
             }
             fence_proxy_async_smem();
-            mbar_arrive(&S.dq_staged);
-            if (tid == 0) {
-                if (!mbar_wait(&S.dq_staged, tt & 1, abort)) return false;
-                tma_reduce_add_3d(&tm_dq, S.dq_stage[0], 0, hh, q_start + qq0);
-                tma_reduce_add_3d(&tm_dq, S.dq_stage[1], 32, hh, q_start + qq0);
-                bulk_commit_group();
-                bulk_wait_read_all();
-                mbar_arrive(&S.dq_stage_free);
-            }
+            mbar_arrive(&S.dq_staged);  // warp 2 adds the staged tile to the accumulator
             return true;
         };
 
@@ -405,7 +412,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xffffffffu, ok);
         const bool have = ok && T > 0;
         if (have) tc_fence_after();
-        if (tid == 0) bulk_wait_all();  // the dQ reduce-adds have landed
         const size_t rowoff = ((size_t)(k_start + kpos) * p.hkv + kvh) * D;
         const uint32_t col = ch == 0 ? cDK : cDV;
         const float f = ch == 0 ? p.scale : 1.f;
