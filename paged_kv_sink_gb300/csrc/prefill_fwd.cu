@@ -21,9 +21,11 @@
 //   warps 4..7  softmax warpgroup; thread = query row.
 // TMEM (256 columns): S at 0, O at 128, P (bf16 pairs) at 192.
 // The online softmax starts from m = sink, l = 1 (the sink costs nothing per
-// tile).  The running reference max is only moved when a tile's max exceeds
-// it by more than 2^8 (then O in TMEM is rescaled in place), which keeps every
-// P value <= 256 and leaves the result exact.
+// tile).  Each tile is first exponentiated against the running reference max
+// without computing its row max; only when the row sum shows a value above
+// 2^64 (or no reference exists yet) is the row max taken and, if it exceeds
+// the reference by more than 2^64, O in TMEM rescaled in place.  P values stay
+// below 2^64, far inside fp32/bf16 range, so the result is exact.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -43,13 +45,17 @@ constexpr int VSTAGE = 2;
 constexpr int kThreads = 256;
 // Two CTAs per SM: 128 registers per thread at launch.  setmaxnreg moves them
 // from warpgroup 0 (TMA + MMA) to the softmax warpgroup:
-// 128*56 + 128*200 = 32768 = 256 threads * 128.
-constexpr int kRegsCtrl = 56;
-constexpr int kRegsSoftmax = 200;
+// 128*40 + 128*216 = 32768 = 256 threads * 128.
+constexpr int kRegsCtrl = 40;
+constexpr int kRegsSoftmax = 216;
 constexpr uint32_t kTile = 128 * 128;  // 128 rows x 128 bytes
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t cS = 0, cO = 128, cP = 192;  // TMEM columns
-constexpr float kRescaleThreshold = 8.0f;        // log2 units
+// The running reference max only moves when a row's max exceeds it by more
+// than 2^64 (log2 units below); every P value stays below 2^64 and every sum
+// far below fp32's range, so the stale reference costs no accuracy.
+constexpr float kRescaleThreshold = 64.0f;
+constexpr float kFastSumLimit = 1.8446744e19f;  // 2^64
 
 struct __align__(1024) Smem {
     uint8_t q[kTile];
@@ -89,9 +95,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Grid (head, request, row tile) with the row tile slowest and reversed: the
+    // last row tiles of every request (the most key tiles under causal masking)
+    // are launched first and short CTAs fill the tail.
     const int h = blockIdx.x;
-    const int rt = p.n_rt - 1 - (int)blockIdx.y;  // heaviest row tiles first
-    const int b = blockIdx.z;
+    const int b = blockIdx.y;
+    const int rt = p.n_rt - 1 - (int)blockIdx.z;
 
     const int q_start = p.cu_q[b];
     int Lq = p.cu_q[b + 1] - q_start;
@@ -275,48 +284,66 @@ __global__ void __launch_bounds__(kThreads, 2)
                         if (!vis) s[c][i] = __float_as_uint(-INFINITY);
                     }
             }
-            // Row max: eight independent 3-input max chains of 16 values.
-            float mc[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const uint32_t* v = &s[k >> 1][(k & 1) * 16];
-                float m = max3f(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
-#pragma unroll
-                for (int i = 3; i < 15; i += 2) m = max3f(m, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
-                mc[k] = fmaxf(m, __uint_as_float(v[15]));
-            }
-            const float mx = max3f(max3f(mc[0], mc[1], mc[2]), max3f(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
-            const float m_new = fmaxf(m_ref, mx * sl2);
-            const bool resc = m_new > m_ref + kRescaleThreshold;
-            const float alpha = resc ? fast_exp2(m_ref - m_new) : 1.f;
-            if (resc) {
-                l *= alpha;
-                m_ref = m_new;
-            }
-            const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-            // P = 2^(s*scale*log2e - m) into registers (packed fp32x2 FMA, MUFU ex2,
+            // P = 2^(s*scale*log2e - m_use) into registers (packed fp32x2 FMA, MUFU ex2,
             // packed partial sums) before waiting for the previous P V.
-            const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(-m_use, -m_use);
-            uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
             uint32_t w[64];
+            auto exps = [&](float m_use) -> float {
+                const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(-m_use, -m_use);
+                uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-            for (int e = 0; e < 64; ++e) {
-                const int i0 = 2 * e;
-                const uint64_t y = f2_fma(f2_pack(__uint_as_float(s[i0 >> 5][i0 & 31]),
-                                                  __uint_as_float(s[(i0 + 1) >> 5][(i0 + 1) & 31])),
-                                          sc2, nm2);
-                float y0, y1;
-                f2_unpack(y, y0, y1);
-                const float x0 = fast_exp2(y0), x1 = fast_exp2(y1);
-                acc2[e & 3] = f2_add(acc2[e & 3], f2_pack(x0, x1));
-                w[e] = pack_bf16x2(x0, x1);
-            }
+                for (int e = 0; e < 64; ++e) {
+                    const int i0 = 2 * e;
+                    const uint64_t y = f2_fma(f2_pack(__uint_as_float(s[i0 >> 5][i0 & 31]),
+                                                      __uint_as_float(s[(i0 + 1) >> 5][(i0 + 1) & 31])),
+                                              sc2, nm2);
+                    float y0, y1;
+                    f2_unpack(y, y0, y1);
+                    const float x0 = fast_exp2(y0), x1 = fast_exp2(y1);
+                    acc2[e & 3] = f2_add(acc2[e & 3], f2_pack(x0, x1));
+                    w[e] = pack_bf16x2(x0, x1);
+                }
+                float sum = 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float lo, hi;
+                    f2_unpack(acc2[e], lo, hi);
+                    sum += lo + hi;
+                }
+                return sum;
+            };
+            // Fast path: exponentiate against the current reference without the row
+            // max.  Every value is then <= 2^64 unless the row sum exceeds 2^64 (or
+            // overflowed), in which case the exact pass redoes the tile.
+            bool resc = false;
+            float alpha = 1.f;
             float rs = 0.f;
+            bool slow = __any_sync(0xffffffffu, m_ref == -INFINITY);
+#pragma unroll 1
+            for (int pass = slow ? 1 : 0; pass < 2; ++pass) {
+                if (pass == 1) {
+                    // Row max: eight independent 3-input max chains of 16 values.
+                    float mc[8];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float lo, hi;
-                f2_unpack(acc2[e], lo, hi);
-                rs += lo + hi;
+                    for (int k = 0; k < 8; ++k) {
+                        const uint32_t* v = &s[k >> 1][(k & 1) * 16];
+                        float m = max3f(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+#pragma unroll
+                        for (int i = 3; i < 15; i += 2)
+                            m = max3f(m, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+                        mc[k] = fmaxf(m, __uint_as_float(v[15]));
+                    }
+                    const float mx =
+                        max3f(max3f(mc[0], mc[1], mc[2]), max3f(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
+                    const float m_new = fmaxf(m_ref, mx * sl2);
+                    resc = m_new > m_ref + kRescaleThreshold;
+                    alpha = resc ? fast_exp2(m_ref - m_new) : 1.f;
+                    if (resc) {
+                        l *= alpha;
+                        m_ref = m_new;
+                    }
+                }
+                rs = exps(m_ref == -INFINITY ? 0.f : m_ref);
+                if (pass == 0 && !__any_sync(0xffffffffu, !(rs <= kFastSumLimit))) break;
             }
             l += rs;
             if (it > 0) {
@@ -456,7 +483,7 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s, std::string* what) {
         *what = "smem attribute";
         return e;
     }
-    dim3 grid(a.hq, p.n_rt, a.batch);
+    dim3 grid(a.hq, a.batch, p.n_rt);
     fwd_kernel<<<grid, kThreads, smem, s>>>(tq, tk, tv, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) *what = "launch";
