@@ -95,12 +95,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // Grid (head, request, row tile) with the row tile slowest and reversed: the
-    // last row tiles of every request (the most key tiles under causal masking)
-    // are launched first and short CTAs fill the tail.
+    // Grid (head, row tile, request): the CTAs in flight share one request's K/V
+    // (it stays in L2); within a request the last row tiles (the most key tiles
+    // under causal masking) are launched first.
     const int h = blockIdx.x;
-    const int b = blockIdx.y;
-    const int rt = p.n_rt - 1 - (int)blockIdx.z;
+    const int rt = p.n_rt - 1 - (int)blockIdx.y;
+    const int b = blockIdx.z;
 
     const int q_start = p.cu_q[b];
     int Lq = p.cu_q[b + 1] - q_start;
@@ -483,7 +483,7 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s, std::string* what) {
         *what = "smem attribute";
         return e;
     }
-    dim3 grid(a.hq, a.batch, p.n_rt);
+    dim3 grid(a.hq, p.n_rt, a.batch);
     fwd_kernel<<<grid, kThreads, smem, s>>>(tq, tk, tv, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) *what = "launch";
