@@ -13,15 +13,15 @@
 //  * bwd_main_kernel (tcgen05): one CTA per (128-key tile, KV head, request);
 //    it loops over the query heads of the KV group and the 128-row query tiles
 //    that see its keys.  Per step five tcgen05 GEMMs:
-//        S^T = K Q^T, dP^T = V dO^T          (TMEM, 128 x 128 fp32 each)
+//        S = Q K^T, dP = dO V^T              (TMEM, 128 x 128 fp32 each)
 //        dV += P^T dO, dK += dS^T Q          (TMEM accumulators over the whole loop)
 //        dQ  = dS K                          (TMEM, double-buffered)
-//    Two warpgroups share the elementwise work: thread = (key row, half of the
-//    128 query columns).  They write P^T and dS^T to shared memory in the
-//    128-byte-swizzled layout (dS^T is read K-major for dK and MN-major, as dS,
-//    for dQ), and add the previous step's dQ tile (TMEM, double-buffered) to an
-//    fp32 accumulator with TMA bulk tensor reduce-adds.  dK/dV are summed over the
-//    group in TMEM (no atomics).
+//    Two warpgroups share the elementwise work: thread = (query row, half of the
+//    128 key columns), so the row's LSE and D are per-thread scalars.  They
+//    write P and dS to shared memory in the 128-byte-swizzled layout (read
+//    MN-major as P^T / dS^T for dV / dK and K-major for dQ), and add the
+//    previous step's dQ tile to an fp32 accumulator with TMA bulk tensor
+//    reduce-adds.  dK/dV are summed over the group in TMEM (no atomics).
 //  * bwd_dq_convert_kernel: fp32 dQ accumulator -> bf16.
 #include <cudaTypedefs.h>
 
@@ -41,6 +41,7 @@ constexpr int kThreads = 384;
 constexpr int kRegsCtrl = 104;
 constexpr int kRegsWork = 200;  // 128*104 + 256*200 = 64512 = 384 * 168
 constexpr int kWork = 256;      // elementwise threads: warps 4..11
+constexpr int kQStages = 3;     // Q / dO ring depth
 constexpr uint32_t kTile = 128 * 128;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns
@@ -49,22 +50,19 @@ constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDK = 320, cDQ = 384;  // dQ: 3
 struct __align__(1024) Smem {
     uint8_t k[kTile];
     uint8_t v[kTile];
-    uint8_t q[2][kTile];
-    uint8_t dout[2][kTile];
-    uint8_t pt[2 * kTile];   // P^T  (128 keys x 128 queries), two 64-query atoms
-    uint8_t dst[2 * kTile];  // dS^T (same layout)
+    uint8_t q[kQStages][kTile];
+    uint8_t dout[kQStages][kTile];
+    uint8_t pb[2 * kTile];   // P  (128 queries x 128 keys): two 64-key atoms of 128-byte rows
+    uint8_t dsb[2 * kTile];  // dS (same layout)
     uint8_t dq_stage[2][kTile];  // dQ tile staging: two 32-column fp32 halves, 128-byte swizzled rows
-    float nlse2[2][BM];      // -LSE * log2(e) of the current query tile (-inf for rows past the end)
-    float nd[2][BM];         // -D of the current query tile (0 past the end)
     uint64_t kv_full;
-    uint64_t qdo_full[2], qdo_empty[2];
+    uint64_t qdo_full[kQStages], qdo_empty[kQStages];
     uint64_t sdp_full, sdp_free, pds_full, mma2_done;  // per step
     uint64_t dq_free[2];
-    uint64_t lse_ready[2];  // the elementwise warps have filled nlse2/nd[buf]
     uint64_t dq_staged;     // all elementwise threads wrote their part of the dQ tile
     uint64_t dq_stage_free; // the bulk reduce has finished reading the staging buffer
     uint64_t final_bar;  // dV / dK / dQ issuer done
-    uint64_t final_sdp;  // S^T / dP^T issuer done
+    uint64_t final_sdp;  // S / dP issuer done
     uint32_t tmem_base;
     int abort;
 };
@@ -111,6 +109,32 @@ __device__ __forceinline__ QRange query_tiles(int j0, int Lq, int Lk, int causal
     return r;
 }
 
+// P = 2^(S scale log2(e) - LSE log2(e)) and dS = P (dP - D) for 32 key columns of
+// one query row, packed to bf16 pairs; kMask zeroes the keys the row does not see
+// (c > c_last, or c_first_end <= c < c_win).
+template <bool kMask>
+__device__ __forceinline__ void p_ds_half(const uint32_t (&sr)[32], const uint32_t (&dr)[32], int col, uint64_t sc2,
+                                          uint64_t nl2x2, uint64_t ndx2, int c_last, int c_first_end, int c_win,
+                                          uint32_t* pw, uint32_t* dw) {
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+        const int c = col + e;
+        float y0, y1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sc2, nl2x2), y0, y1);
+        float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
+        if (kMask) {
+            if (c > c_last || (c >= c_first_end && c < c_win)) p0 = 0.f;
+            if (c + 1 > c_last || (c + 1 >= c_first_end && c + 1 < c_win)) p1 = 0.f;
+        }
+        const uint64_t ds = f2_mul(f2_pack(p0, p1),
+                                   f2_add(f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), ndx2));
+        float d0, d1;
+        f2_unpack(ds, d0, d1);
+        pw[e >> 1] = pack_bf16x2(p0, p1);
+        dw[e >> 1] = pack_bf16x2(d0, d1);
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -141,12 +165,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(&S.kv_full, 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kQStages; ++s) {
             mbar_init(&S.qdo_full[s], 1);
             mbar_init(&S.qdo_empty[s], 1);
-            mbar_init(&S.dq_free[s], kWork);
-            mbar_init(&S.lse_ready[s], kWork);
         }
+        for (int s = 0; s < 2; ++s) mbar_init(&S.dq_free[s], kWork);
         mbar_init(&S.sdp_full, 1);
         mbar_init(&S.sdp_free, kWork);
         mbar_init(&S.pds_full, kWork);
@@ -181,8 +204,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(S.v, &tm_v, &S.kv_full, 0, kvh, k_start + j0);
             int t = 0;
             for (; t < T; ++t) {
-                const int st = t & 1;
-                if (t >= 2 && !mbar_wait(&S.qdo_empty[st], ((t >> 1) - 1) & 1, abort)) break;
+                const int st = t % kQStages;
+                if (t >= kQStages && !mbar_wait(&S.qdo_empty[st], (t / kQStages - 1) & 1, abort)) break;
                 const int h = kvh * p.group + t / nqt;
                 const int q0 = (qr.lo + t % nqt) * BM;
                 mbar_expect_tx(&S.qdo_full[st], 2 * kTile);
@@ -190,8 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(S.dout[st], &tm_do, &S.qdo_full[st], 0, h, q_start + q0);
             }
             drain_wait(&S.kv_full, 0);
-            for (int st = 0; st < 2; ++st) {
-                const int n = t > st ? (t - st + 1) / 2 : 0;
+            for (int st = 0; st < kQStages; ++st) {
+                const int n = t > st ? (t - st + kQStages - 1) / kQStages : 0;  // loads issued into stage st
                 if (n > 0) drain_wait(&S.qdo_full[st], (n - 1) & 1);
             }
         } else if (warp == 2 && lane == 0 && T > 0) {
@@ -212,29 +235,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if ((warp == 1 || warp == 3) && lane == 0 && T > 0) {
             // -------------------------------------------------------- MMA issuers
             // Two issue threads feed the tensor core independent instruction
-            // streams: warp 1 issues each step's S^T / dP^T as soon as the
+            // streams: warp 1 issues each step's S / dP as soon as the
             // elementwise warps have read the previous ones; warp 3 issues the
-            // step's dV / dK / dQ once P^T and dS^T are in shared memory.
-            // Within each stream the independent accumulator chains are
-            // interleaved k-step by k-step.
-            constexpr uint32_t idSS = idesc_bf16_f32(BN, BM, false, false);  // S^T, dP^T
-            constexpr uint32_t idKN = idesc_bf16_f32(BN, D, false, true);    // dV, dK: A K-major, B MN-major
-            constexpr uint32_t idQ = idesc_bf16_f32(BM, D, true, true);      // dQ: A (dS) MN-major, B (K) MN-major
+            // step's dV / dK / dQ once P and dS are in shared memory.  Within
+            // each stream the independent accumulator chains are interleaved
+            // k-step by k-step.
+            constexpr uint32_t idSS = idesc_bf16_f32(BM, BN, false, false);  // S, dP: both K-major
+            constexpr uint32_t idKV = idesc_bf16_f32(BN, D, true, true);     // dV, dK: A (P^T, dS^T) MN-major
+            constexpr uint32_t idQ = idesc_bf16_f32(BM, D, false, true);     // dQ: A (dS) K-major, B (K) MN-major
             const uint32_t sk = smem_u32(S.k), sv = smem_u32(S.v);
-            const uint32_t spt = smem_u32(S.pt), sds = smem_u32(S.dst);
+            const uint32_t spb = smem_u32(S.pb), sdsb = smem_u32(S.dsb);
             bool ok = mbar_wait(&S.kv_full, 0, abort);
             if (warp == 1) {
                 for (int t = 0; ok && t < T; ++t) {
-                    if (!(ok = mbar_wait(&S.qdo_full[t & 1], (t >> 1) & 1, abort))) break;
+                    const int st = t % kQStages;
+                    if (!(ok = mbar_wait(&S.qdo_full[st], (t / kQStages) & 1, abort))) break;
                     if (t > 0 && !(ok = mbar_wait(&S.sdp_free, (t - 1) & 1, abort))) break;
                     tc_fence_after();
-                    const uint32_t sq = smem_u32(S.q[t & 1]), sdo = smem_u32(S.dout[t & 1]);
+                    const uint32_t sq = smem_u32(S.q[st]), sdo = smem_u32(S.dout[st]);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
-                        umma_ss(tmem + cS, sdesc_sw128(sk + kk * 32, 16, 1024), sdesc_sw128(sq + kk * 32, 16, 1024),
+                        umma_ss(tmem + cS, sdesc_sw128(sq + kk * 32, 16, 1024), sdesc_sw128(sk + kk * 32, 16, 1024),
                                 idSS, kk > 0);
-                        umma_ss(tmem + cDP, sdesc_sw128(sv + kk * 32, 16, 1024),
-                                sdesc_sw128(sdo + kk * 32, 16, 1024), idSS, kk > 0);
+                        umma_ss(tmem + cDP, sdesc_sw128(sdo + kk * 32, 16, 1024),
+                                sdesc_sw128(sv + kk * 32, 16, 1024), idSS, kk > 0);
                     }
                     umma_commit(&S.sdp_full);
                 }
@@ -243,23 +267,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 drain_wait(&S.final_sdp, 0);
             } else {
                 for (int t = 0; ok && t < T; ++t) {
-                    const int st = t & 1;
+                    const int st = t % kQStages;
                     if (!(ok = mbar_wait(&S.pds_full, t & 1, abort))) break;
-                    if (t >= 2 && !(ok = mbar_wait(&S.dq_free[st], ((t >> 1) - 1) & 1, abort))) break;
+                    if (t >= 2 && !(ok = mbar_wait(&S.dq_free[t & 1], ((t >> 1) - 1) & 1, abort))) break;
                     tc_fence_after();
                     const uint32_t sq = smem_u32(S.q[st]), sdo = smem_u32(S.dout[st]);
 #pragma unroll
-                    for (int kk = 0; kk < BM / 16; ++kk) {
-                        const uint32_t koff = (kk >> 2) * kTile + (kk & 3) * 32;  // K-major step over queries
-                        const uint32_t moff = kk * 2048;                          // MN-major step over K rows
+                    for (int kk = 0; kk < 8; ++kk) {
+                        // dV / dK: k-step kk runs over query rows 16 kk .. 16 kk + 15 of P / dS
+                        // (rows of the MN-major A and of the MN-major B alike)
+                        const uint32_t moff = kk * 2048;
                         const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
-                        umma_ss(tmem + cDV, sdesc_sw128(spt + koff, 16, 1024), sdesc_sw128(sdo + moff, 8192, 1024),
-                                idKN, acc);
-                        umma_ss(tmem + cDK, sdesc_sw128(sds + koff, 16, 1024), sdesc_sw128(sq + moff, 8192, 1024),
-                                idKN, acc);
-                        // dQ k-step kk runs over keys 16 kk .. 16 kk + 15 (BN == BM)
-                        umma_ss(tmem + cDQ + st * D, sdesc_sw128(sds + kk * 2048, kTile, 1024),
-                                sdesc_sw128(sk + kk * 2048, 8192, 1024), idQ, kk > 0);
+                        umma_ss(tmem + cDV, sdesc_sw128(spb + moff, kTile, 1024), sdesc_sw128(sdo + moff, 8192, 1024),
+                                idKV, acc);
+                        umma_ss(tmem + cDK, sdesc_sw128(sdsb + moff, kTile, 1024), sdesc_sw128(sq + moff, 8192, 1024),
+                                idKV, acc);
+                        // dQ: k-step kk runs over keys 16 kk .. 16 kk + 15 (K-major A, MN-major B)
+                        const uint32_t koff = (kk >> 2) * kTile + (kk & 3) * 32;
+                        umma_ss(tmem + cDQ + (t & 1) * D, sdesc_sw128(sdsb + koff, 16, 1024),
+                                sdesc_sw128(sk + moff, 8192, 1024), idQ, kk > 0);
                     }
                     umma_commit(&S.mma2_done);
                     umma_commit(&S.qdo_empty[st]);
@@ -271,20 +297,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsWork));
         // ------------------------------------------------------------ elementwise
+        // Lane = query row i of the tile (TMEM lanes of S, dP and dQ) and key row
+        // i of the CTA (TMEM lanes of dK, dV); column half ch = keys [64 ch, 64 ch + 64).
         const int q4 = warp & 3;
-        const int ch = (warp - 4) >> 2;      // query-column half: [64 ch, 64 ch + 64)
-        const int j = q4 * 32 + lane;        // key row (P^T/dS^T) and query row (dQ) of this lane
+        const int ch = (warp - 4) >> 2;
+        const int i = q4 * 32 + lane;
         const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
-        const int kpos = j0 + j;
-        const int tid = threadIdx.x - 128;   // 0..255
         const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
+        const int F = p.win_first, W = p.win_last;
         bool ok = true;
 
         // dQ of step tt (its GEMMs are complete): this lane's query row, 32 columns
         // (half ch), staged in shared memory; warp 2 adds the tile to the fp32
         // accumulator with TMA bulk reduce-adds.
         auto flush_dq = [&](int tt) -> bool {
-            const int hh = kvh * p.group + tt / nqt;
             const int qq0 = (qr.lo + tt % nqt) * BM;
             uint32_t u[32];
             tmem_ld32(tmem + lane_base + cDQ + (tt & 1) * D + ch * 32, u);
@@ -293,11 +319,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&S.dq_free[tt & 1]);
             bool fine = tt == 0 || mbar_wait(&S.dq_stage_free, (tt - 1) & 1, abort);
             if (!__all_sync(0xffffffffu, fine)) return false;
-            const float f = qq0 + j < Lq ? p.scale : 0.f;  // rows past the request add zero
+            const float f = qq0 + i < Lq ? p.scale : 0.f;  // rows past the request add zero
             uint8_t* stage = S.dq_stage[ch];
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(smem_u32(stage + sw128_off(j, c))),
+                asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(smem_u32(stage + sw128_off(i, c))),
                              "f"(__uint_as_float(u[4 * c]) * f), "f"(__uint_as_float(u[4 * c + 1]) * f),
                              "f"(__uint_as_float(u[4 * c + 2]) * f), "f"(__uint_as_float(u[4 * c + 3]) * f)
                              : "memory");
@@ -306,23 +332,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&S.dq_staged);  // warp 2 adds the staged tile to the accumulator
             return true;
         };
-
-        for (int t = 0; t < T; ++t) {
-            const int g = t / nqt;
-            const int h = kvh * p.group + g;
-            const int q0 = (qr.lo + t % nqt) * BM;
-            const int buf = t & 1;
-            {  // this query tile's -LSE (log2 units) and -D: threads 0..127 / 128..255
-                const int c = tid & (BM - 1);
-                const int row = q0 + c;
-                if (tid < BM)
-                    S.nlse2[buf][c] = row < Lq ? -p.lse[(size_t)h * p.total_q + q_start + row] * ATTN_LOG2E
-                                               : -INFINITY;
-                else
-                    S.nd[buf][c] = row < Lq ? -p.dvec[(size_t)h * p.total_q + q_start + row] : 0.f;
+        // LSE and D of this lane's query row at step tt (+inf / 0 past the request's end)
+        auto load_row = [&](int tt, float& lse, float& dd) {
+            const int hh = kvh * p.group + tt / nqt;
+            const int row = (qr.lo + tt % nqt) * BM + i;
+            lse = INFINITY;
+            dd = 0.f;
+            if (tt < T && row < Lq) {
+                const size_t at = (size_t)hh * p.total_q + q_start + row;
+                lse = __ldg(p.lse + at);
+                dd = __ldg(p.dvec + at);
             }
-            mbar_arrive(&S.lse_ready[buf]);
-            ok = mbar_wait(&S.lse_ready[buf], (t >> 1) & 1, abort) && mbar_wait(&S.sdp_full, t & 1, abort);
+        };
+
+        float lse_cur, d_cur;
+        load_row(0, lse_cur, d_cur);
+        for (int t = 0; t < T; ++t) {
+            const int q0 = (qr.lo + t % nqt) * BM;
+            float lse_nxt, d_nxt;
+            load_row(t + 1, lse_nxt, d_nxt);  // in flight while this step computes
+            ok = mbar_wait(&S.sdp_full, t & 1, abort);
             if (!__all_sync(0xffffffffu, ok)) {
                 ok = false;
                 break;
@@ -332,12 +361,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int P0 = off + q0, P1 = off + q0 + rows_valid - 1;
             const int jmax = j0 + BN - 1;
             const bool full = (!p.causal || jmax <= P0) && (jmax < Lk) &&
-                              (p.win_last <= 0 || jmax < p.win_first || j0 >= P1 + 1 - p.win_last);
-            // visible query columns of this key: c in [c_lo, c_hi]
-            const int c_lo = p.causal ? kpos - off - q0 : 0;
-            int c_hi = (p.win_last > 0 && kpos >= p.win_first) ? kpos - off - q0 + p.win_last - 1 : BM;
-            if (kpos >= Lk) c_hi = -1;
-            uint32_t pw[32], dw[32];  // packed bf16 P^T and dS^T of this key row, 64 query columns
+                              (W <= 0 || jmax < F || j0 >= P1 + 1 - W);
+            // visible key columns of this query: c <= c_last and (c < c_first_end or c >= c_win)
+            const int qpos = off + q0 + i;
+            const int c_last = min(Lk - 1, p.causal ? qpos : Lk - 1) - j0;
+            const int c_first_end = W > 0 ? F - j0 : BN;
+            const int c_win = W > 0 ? qpos + 1 - W - j0 : 0;
+            const float nl2 = -lse_cur * ATTN_LOG2E;  // -inf past the end: P = 0 there
+            const uint64_t nl2x2 = f2_pack(nl2, nl2);
+            const uint64_t ndx2 = f2_pack(-d_cur, -d_cur);
+            uint32_t pw[32], dw[32];  // packed bf16 P and dS of this query row, 64 key columns
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 uint32_t sr[32], dr[32];
@@ -345,46 +378,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(tmem + lane_base + cS + col, sr);
                 tmem_ld32(tmem + lane_base + cDP + col, dr);
                 tmem_ld_wait();
-                if (half == 1) {  // S^T / dP^T fully read: the next step may overwrite them
+                if (half == 1) {  // S / dP fully read: the next step may overwrite them
                     tc_fence_before();
                     mbar_arrive(&S.sdp_free);
                 }
-#pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    const int c = col + i;
-                    const uint64_t nl = *reinterpret_cast<const uint64_t*>(&S.nlse2[buf][c]);
-                    const uint64_t nd = *reinterpret_cast<const uint64_t*>(&S.nd[buf][c]);
-                    float y0, y1;
-                    f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), sc2, nl), y0, y1);
-                    float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
-                    if (!full) {
-                        if (c < c_lo || c > c_hi) p0 = 0.f;
-                        if (c + 1 < c_lo || c + 1 > c_hi) p1 = 0.f;
-                    }
-                    const uint64_t p01 = f2_pack(p0, p1);
-                    const uint64_t ds =
-                        f2_mul(p01, f2_add(f2_pack(__uint_as_float(dr[i]), __uint_as_float(dr[i + 1])), nd));
-                    float d0, d1;
-                    f2_unpack(ds, d0, d1);
-                    pw[(half * 32 + i) >> 1] = pack_bf16x2(p0, p1);
-                    dw[(half * 32 + i) >> 1] = pack_bf16x2(d0, d1);
-                }
+                if (full)
+                    p_ds_half<false>(sr, dr, col, sc2, nl2x2, ndx2, c_last, c_first_end, c_win, pw + half * 16,
+                                     dw + half * 16);
+                else
+                    p_ds_half<true>(sr, dr, col, sc2, nl2x2, ndx2, c_last, c_first_end, c_win, pw + half * 16,
+                                    dw + half * 16);
             }
-            if (t > 0) {  // the previous step's GEMMs must be done reading P^T / dS^T
+            if (t > 0) {  // the previous step's GEMMs must be done reading P / dS
                 ok = mbar_wait(&S.mma2_done, (t - 1) & 1, abort);
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
                     break;
                 }
             }
-            // 64 query columns = atom ch, chunks 0..7 of 16 bytes
+            // 64 key columns = atom ch, chunks 0..7 of 16 bytes
 #pragma unroll
             for (int cc = 0; cc < 8; ++cc) {
-                const uint32_t o = ch * kTile + sw128_off(j, cc);
-                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(smem_u32(S.pt + o)), "r"(pw[4 * cc]),
+                const uint32_t o = ch * kTile + sw128_off(i, cc);
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(smem_u32(S.pb + o)), "r"(pw[4 * cc]),
                              "r"(pw[4 * cc + 1]), "r"(pw[4 * cc + 2]), "r"(pw[4 * cc + 3])
                              : "memory");
-                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(smem_u32(S.dst + o)), "r"(dw[4 * cc]),
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(smem_u32(S.dsb + o)), "r"(dw[4 * cc]),
                              "r"(dw[4 * cc + 1]), "r"(dw[4 * cc + 2]), "r"(dw[4 * cc + 3])
                              : "memory");
             }
@@ -398,6 +417,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
             }
+            lse_cur = lse_nxt;
+            d_cur = d_nxt;
         }
         // last step's dQ, then dK (column half 0) / dV (column half 1)
         if (ok && T > 0) {
@@ -412,6 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xffffffffu, ok);
         const bool have = ok && T > 0;
         if (have) tc_fence_after();
+        const int kpos = j0 + i;
         const size_t rowoff = ((size_t)(k_start + kpos) * p.hkv + kvh) * D;
         const uint32_t col = ch == 0 ? cDK : cDV;
         const float f = ch == 0 ? p.scale : 1.f;
@@ -424,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_wait();
             } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) u[i] = 0u;
+                for (int e = 0; e < 32; ++e) u[e] = 0u;
             }
             if (kpos < Lk) {
                 uint4* dst = reinterpret_cast<uint4*>(outp + rowoff + half * 32);
