@@ -232,65 +232,72 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&S.dq_stage_free);
             }
             bulk_wait_all();  // the reduce-adds have landed before the CTA exits
-        } else if ((warp == 1 || warp == 3) && lane == 0 && T > 0) {
+        } else if ((warp == 1 || warp == 3) && T > 0) {
             // -------------------------------------------------------- MMA issuers
-            // Two issue threads feed the tensor core independent instruction
+            // Two issuing warps feed the tensor core independent instruction
             // streams: warp 1 issues each step's S / dP as soon as the
             // elementwise warps have read the previous ones; warp 3 issues the
-            // step's dV / dK / dQ once P and dS are in shared memory.  Within
-            // each stream the independent accumulator chains are interleaved
-            // k-step by k-step.
+            // step's dV / dK / dQ once P and dS are in shared memory.  Both run
+            // converged (every lane waits; elect.sync picks the issuing lane),
+            // and within a stream the independent accumulator chains are
+            // interleaved k-step by k-step.
             constexpr uint32_t idSS = idesc_bf16_f32(BM, BN, false, false);  // S, dP: both K-major
             constexpr uint32_t idKV = idesc_bf16_f32(BN, D, true, true);     // dV, dK: A (P^T, dS^T) MN-major
             constexpr uint32_t idQ = idesc_bf16_f32(BM, D, false, true);     // dQ: A (dS) K-major, B (K) MN-major
-            const uint32_t sk = smem_u32(S.k), sv = smem_u32(S.v);
-            const uint32_t spb = smem_u32(S.pb), sdsb = smem_u32(S.dsb);
-            bool ok = mbar_wait(&S.kv_full, 0, abort);
+            // Descriptor bases; a k-step adds its byte offset / 16 to the address field.
+            const uint64_t dk_k = sdesc_sw128(smem_u32(S.k), 16, 1024);        // K, K-major (B of S)
+            const uint64_t dv_k = sdesc_sw128(smem_u32(S.v), 16, 1024);        // V, K-major (B of dP)
+            const uint64_t dk_mn = sdesc_sw128(smem_u32(S.k), 8192, 1024);     // K, MN-major (B of dQ)
+            const uint64_t dp_mn = sdesc_sw128(smem_u32(S.pb), kTile, 1024);   // P^T, MN-major (A of dV)
+            const uint64_t ds_mn = sdesc_sw128(smem_u32(S.dsb), kTile, 1024);  // dS^T, MN-major (A of dK)
+            const uint64_t ds_k = sdesc_sw128(smem_u32(S.dsb), 16, 1024);      // dS, K-major (A of dQ)
+            auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+                return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
+            };
+            bool ok = wait_all(&S.kv_full, 0);
             if (warp == 1) {
                 for (int t = 0; ok && t < T; ++t) {
                     const int st = t % kQStages;
-                    if (!(ok = mbar_wait(&S.qdo_full[st], (t / kQStages) & 1, abort))) break;
-                    if (t > 0 && !(ok = mbar_wait(&S.sdp_free, (t - 1) & 1, abort))) break;
+                    if (!(ok = wait_all(&S.qdo_full[st], (t / kQStages) & 1))) break;
+                    if (t > 0 && !(ok = wait_all(&S.sdp_free, (t - 1) & 1))) break;
                     tc_fence_after();
-                    const uint32_t sq = smem_u32(S.q[st]), sdo = smem_u32(S.dout[st]);
+                    const uint64_t dq_k = sdesc_sw128(smem_u32(S.q[st]), 16, 1024);
+                    const uint64_t ddo_k = sdesc_sw128(smem_u32(S.dout[st]), 16, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        umma_ss(tmem + cS, sdesc_sw128(sq + kk * 32, 16, 1024), sdesc_sw128(sk + kk * 32, 16, 1024),
-                                idSS, kk > 0);
-                        umma_ss(tmem + cDP, sdesc_sw128(sdo + kk * 32, 16, 1024),
-                                sdesc_sw128(sv + kk * 32, 16, 1024), idSS, kk > 0);
+                    for (int kk = 0; kk < D / 16; ++kk) {  // 16 head-dim elements = 32 bytes per k-step
+                        umma_ss_e(tmem + cS, dq_k + 2 * kk, dk_k + 2 * kk, idSS, kk > 0);
+                        umma_ss_e(tmem + cDP, ddo_k + 2 * kk, dv_k + 2 * kk, idSS, kk > 0);
                     }
-                    umma_commit(&S.sdp_full);
+                    umma_commit_e(&S.sdp_full);
                 }
-                // Every MMA this thread issued must be complete before TMEM is released.
-                umma_commit(&S.final_sdp);
+                // Every MMA this warp issued must be complete before TMEM is released.
+                umma_commit_e(&S.final_sdp);
                 drain_wait(&S.final_sdp, 0);
             } else {
                 for (int t = 0; ok && t < T; ++t) {
                     const int st = t % kQStages;
-                    if (!(ok = mbar_wait(&S.pds_full, t & 1, abort))) break;
-                    if (t >= 2 && !(ok = mbar_wait(&S.dq_free[t & 1], ((t >> 1) - 1) & 1, abort))) break;
+                    if (!(ok = wait_all(&S.pds_full, t & 1))) break;
+                    if (t >= 2 && !(ok = wait_all(&S.dq_free[t & 1], ((t >> 1) - 1) & 1))) break;
                     tc_fence_after();
-                    const uint32_t sq = smem_u32(S.q[st]), sdo = smem_u32(S.dout[st]);
+                    const uint64_t dq_mn = sdesc_sw128(smem_u32(S.q[st]), 8192, 1024);
+                    const uint64_t ddo_mn = sdesc_sw128(smem_u32(S.dout[st]), 8192, 1024);
+                    const uint32_t cq = tmem + cDQ + (t & 1) * D;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         // dV / dK: k-step kk runs over query rows 16 kk .. 16 kk + 15 of P / dS
-                        // (rows of the MN-major A and of the MN-major B alike)
-                        const uint32_t moff = kk * 2048;
+                        // (2048 bytes into the MN-major A and B alike)
                         const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
-                        umma_ss(tmem + cDV, sdesc_sw128(spb + moff, kTile, 1024), sdesc_sw128(sdo + moff, 8192, 1024),
-                                idKV, acc);
-                        umma_ss(tmem + cDK, sdesc_sw128(sdsb + moff, kTile, 1024), sdesc_sw128(sq + moff, 8192, 1024),
-                                idKV, acc);
-                        // dQ: k-step kk runs over keys 16 kk .. 16 kk + 15 (K-major A, MN-major B)
-                        const uint32_t koff = (kk >> 2) * kTile + (kk & 3) * 32;
-                        umma_ss(tmem + cDQ + (t & 1) * D, sdesc_sw128(sdsb + koff, 16, 1024),
-                                sdesc_sw128(sk + moff, 8192, 1024), idQ, kk > 0);
+                        umma_ss_e(tmem + cDV, dp_mn + 128 * kk, ddo_mn + 128 * kk, idKV, acc);
+                        umma_ss_e(tmem + cDK, ds_mn + 128 * kk, dq_mn + 128 * kk, idKV, acc);
+                        // dQ: k-step kk runs over keys 16 kk .. 16 kk + 15 (K-major dS: 64-key atom
+                        // kk / 4, 32 bytes per step inside it; MN-major K: 2048 bytes per step)
+                        umma_ss_e(cq, ds_k + (kk >> 2) * (kTile >> 4) + (kk & 3) * 2, dk_mn + 128 * kk, idQ,
+                                  kk > 0);
                     }
-                    umma_commit(&S.mma2_done);
-                    umma_commit(&S.qdo_empty[st]);
+                    umma_commit_e(&S.mma2_done);
+                    umma_commit_e(&S.qdo_empty[st]);
                 }
-                umma_commit(&S.final_bar);
+                umma_commit_e(&S.final_bar);
                 drain_wait(&S.final_bar, 0);
             }
         }

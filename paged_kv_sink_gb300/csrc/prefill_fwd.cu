@@ -191,21 +191,28 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int n = it > st ? (it - st + nst - 1) / nst : 0;
                 if (n > 0) drain_wait(&full[st], (n - 1) & 1);
             }
-        } else if (warp == 1 && lane == 0 && ntiles > 0) {
+        } else if (warp == 1 && ntiles > 0) {
             // -------------------------------------------------------- MMA issuer
+            // The whole warp runs the loop converged (every lane waits;
+            // elect.sync picks the issuing lane).
             constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false, false);
             constexpr uint32_t idO = idesc_bf16_f32(BM, D, false, true);
-            const uint32_t sq = smem_u32(S.q), sk = smem_u32(S.k[0]), sv = smem_u32(S.v[0]);
-            auto issue_S = [&](int it) {
-                const uint32_t kb = sk + (it % KSTAGE) * kTile;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    umma_ss(tmem + cS, sdesc_sw128(sq + kk * 32, 16, 1024), sdesc_sw128(kb + kk * 32, 16, 1024),
-                            idS, kk > 0);
-                umma_commit(&S.s_full);
-                umma_commit(&S.k_empty[it % KSTAGE]);
+            // Descriptor bases; a k-step adds its byte offset / 16 to the address field.
+            const uint64_t dq = sdesc_sw128(smem_u32(S.q), 16, 1024);
+            const uint64_t dk0 = sdesc_sw128(smem_u32(S.k[0]), 16, 1024);
+            const uint64_t dv0 = sdesc_sw128(smem_u32(S.v[0]), 8192, 1024);
+            auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+                return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
             };
-            bool ok = mbar_wait(&S.q_full, 0, abort) && mbar_wait(&S.k_full[0], 0, abort);
+            auto issue_S = [&](int it) {
+                const uint64_t dk = dk0 + (it % KSTAGE) * (kTile >> 4);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)  // 16 head-dim elements = 32 bytes per k-step
+                    umma_ss_e(tmem + cS, dq + 2 * kk, dk + 2 * kk, idS, kk > 0);
+                umma_commit_e(&S.s_full);
+                umma_commit_e(&S.k_empty[it % KSTAGE]);
+            };
+            bool ok = wait_all(&S.q_full, 0) && wait_all(&S.k_full[0], 0);
             if (ok) {
                 tc_fence_after();
                 issue_S(0);
@@ -215,25 +222,25 @@ __global__ void __launch_bounds__(kThreads, 2)
                 // The next S as soon as the softmax has read this one (it runs on
                 // the tensor core while the softmax works) ...
                 if (nx < ntiles) {
-                    if (!(ok = mbar_wait(&S.k_full[nx % KSTAGE], (nx / KSTAGE) & 1, abort))) break;
-                    if (!(ok = mbar_wait(&S.s_free, it & 1, abort))) break;
+                    if (!(ok = wait_all(&S.k_full[nx % KSTAGE], (nx / KSTAGE) & 1))) break;
+                    if (!(ok = wait_all(&S.s_free, it & 1))) break;
                     tc_fence_after();
                     issue_S(nx);
                 }
-                // ... then O += P V once P is in TMEM (8 columns of bf16 pairs per 16 keys).
-                if (!(ok = mbar_wait(&S.v_full[it % VSTAGE], (it / VSTAGE) & 1, abort))) break;
-                if (!(ok = mbar_wait(&S.p_full, it & 1, abort))) break;
+                // ... then O += P V once P is in TMEM (8 columns of bf16 pairs per 16 keys;
+                // V rows 2048 bytes on per 16 keys).
+                if (!(ok = wait_all(&S.v_full[it % VSTAGE], (it / VSTAGE) & 1))) break;
+                if (!(ok = wait_all(&S.p_full, it & 1))) break;
                 tc_fence_after();
-                const uint32_t vb = sv + (it % VSTAGE) * kTile;
+                const uint64_t dv = dv0 + (it % VSTAGE) * (kTile >> 4);
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
-                    umma_ts(tmem + cO, tmem + cP + kk * 8, sdesc_sw128(vb + kk * 2048, 8192, 1024), idO,
-                            (it > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(&S.o_done);
-                umma_commit(&S.v_empty[it % VSTAGE]);
+                    umma_ts_e(tmem + cO, tmem + cP + kk * 8, dv + 128 * kk, idO, (it > 0 || kk > 0) ? 1u : 0u);
+                umma_commit_e(&S.o_done);
+                umma_commit_e(&S.v_empty[it % VSTAGE]);
             }
             // Every MMA issued must be complete before TMEM is released.
-            umma_commit(&S.final_bar);
+            umma_commit_e(&S.final_bar);
             drain_wait(&S.final_bar, 0);
         }
     } else {
