@@ -317,8 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dQ of step tt (its GEMMs are complete): this lane's query row, 32 columns
         // (half ch), staged in shared memory; warp 2 adds the tile to the fp32
         // accumulator with TMA bulk reduce-adds.
-        auto flush_dq = [&](int tt) -> bool {
-            const int qq0 = (qr.lo + tt % nqt) * BM;
+        auto flush_dq = [&](int tt, int qq0) -> bool {
             uint32_t u[32];
             tmem_ld32(tmem + lane_base + cDQ + (tt & 1) * D + ch * 32, u);
             tmem_ld_wait();
@@ -339,25 +338,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&S.dq_staged);  // warp 2 adds the staged tile to the accumulator
             return true;
         };
-        // LSE and D of this lane's query row at step tt (+inf / 0 past the request's end)
-        auto load_row = [&](int tt, float& lse, float& dd) {
-            const int hh = kvh * p.group + tt / nqt;
-            const int row = (qr.lo + tt % nqt) * BM + i;
+        // LSE and D of this lane's query row for head g of the group and query tile
+        // qt (+inf / 0 past the request's end and past the last step)
+        auto load_row = [&](int g, int qt, float& lse, float& dd) {
+            const int row = (qr.lo + qt) * BM + i;
             lse = INFINITY;
             dd = 0.f;
-            if (tt < T && row < Lq) {
-                const size_t at = (size_t)hh * p.total_q + q_start + row;
+            if (g < p.group && row < Lq) {
+                const size_t at = (size_t)(kvh * p.group + g) * p.total_q + q_start + row;
                 lse = __ldg(p.lse + at);
                 dd = __ldg(p.dvec + at);
             }
         };
 
+        // step t = g_c * nqt + qt_c (head g_c of the group, query tile qt_c)
+        int g_c = 0, qt_c = 0, q0_prev = 0;
         float lse_cur, d_cur;
-        load_row(0, lse_cur, d_cur);
+        load_row(0, 0, lse_cur, d_cur);
         for (int t = 0; t < T; ++t) {
-            const int q0 = (qr.lo + t % nqt) * BM;
+            const int q0 = (qr.lo + qt_c) * BM;
+            int g_n = g_c, qt_n = qt_c + 1;
+            if (qt_n == nqt) {
+                qt_n = 0;
+                ++g_n;
+            }
             float lse_nxt, d_nxt;
-            load_row(t + 1, lse_nxt, d_nxt);  // in flight while this step computes
+            load_row(g_n, qt_n, lse_nxt, d_nxt);  // in flight while this step computes
             ok = mbar_wait(&S.sdp_full, t & 1, abort);
             if (!__all_sync(0xffffffffu, ok)) {
                 ok = false;
@@ -419,13 +425,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&S.pds_full);
             if (t > 0) {
                 tc_fence_after();
-                if (!__all_sync(0xffffffffu, flush_dq(t - 1))) {
+                if (!__all_sync(0xffffffffu, flush_dq(t - 1, q0_prev))) {
                     ok = false;
                     break;
                 }
             }
             lse_cur = lse_nxt;
             d_cur = d_nxt;
+            q0_prev = q0;
+            g_c = g_n;
+            qt_c = qt_n;
         }
         // last step's dQ, then dK (column half 0) / dV (column half 1)
         if (ok && T > 0) {
@@ -433,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
                 tc_fence_after();
-                ok = __all_sync(0xffffffffu, flush_dq(T - 1));
+                ok = __all_sync(0xffffffffu, flush_dq(T - 1, q0_prev));
             }
         }
         if (ok && T > 0) ok = mbar_wait(&S.final_bar, 0, abort);
