@@ -18,7 +18,7 @@
 //        dQ  = dS K                          (TMEM, double-buffered)
 //    Two warpgroups share the elementwise work: thread = (query row, half of the
 //    128 key columns), so the row's LSE and D are per-thread scalars.  They
-//    write P and dS to shared memory in the 128-byte-swizzled layout (read
+//    write P and scale dS to shared memory in the 128-byte-swizzled layout (read
 //    MN-major as P^T / dS^T for dV / dK and K-major for dQ), and add the
 //    previous step's dQ tile to an fp32 accumulator with TMA bulk tensor
 //    reduce-adds.  dK/dV are summed over the group in TMEM (no atomics).
@@ -114,8 +114,8 @@ __device__ __forceinline__ QRange query_tiles(int j0, int Lq, int Lk, int causal
 // (c > c_last, or c_first_end <= c < c_win).
 template <bool kMask>
 __device__ __forceinline__ void p_ds_half(const uint32_t (&sr)[32], const uint32_t (&dr)[32], int col, uint64_t sc2,
-                                          uint64_t nl2x2, uint64_t ndx2, int c_last, int c_first_end, int c_win,
-                                          uint32_t* pw, uint32_t* dw) {
+                                          uint64_t nl2x2, uint64_t scx2, uint64_t ndx2, int c_last, int c_first_end,
+                                          int c_win, uint32_t* pw, uint32_t* dw) {
 #pragma unroll
     for (int e = 0; e < 32; e += 2) {
         const int c = col + e;
@@ -127,7 +127,7 @@ __device__ __forceinline__ void p_ds_half(const uint32_t (&sr)[32], const uint32
             if (c + 1 > c_last || (c + 1 >= c_first_end && c + 1 < c_win)) p1 = 0.f;
         }
         const uint64_t ds = f2_mul(f2_pack(p0, p1),
-                                   f2_add(f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), ndx2));
+                                   f2_fma(f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), scx2, ndx2));
         float d0, d1;
         f2_unpack(ds, d0, d1);
         pw[e >> 1] = pack_bf16x2(p0, p1);
@@ -311,32 +311,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i = q4 * 32 + lane;
         const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
         const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
+        const uint64_t scx2 = f2_pack(p.scale, p.scale);
         const int F = p.win_first, W = p.win_last;
         bool ok = true;
 
-        // dQ of step tt (its GEMMs are complete): this lane's query row, 32 columns
-        // (half ch), staged in shared memory; warp 2 adds the tile to the fp32
-        // accumulator with TMA bulk reduce-adds.
-        auto flush_dq = [&](int tt, int qq0) -> bool {
-            uint32_t u[32];
-            tmem_ld32(tmem + lane_base + cDQ + (tt & 1) * D + ch * 32, u);
-            tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(&S.dq_free[tt & 1]);
-            bool fine = tt == 0 || mbar_wait(&S.dq_stage_free, (tt - 1) & 1, abort);
-            if (!__all_sync(0xffffffffu, fine)) return false;
-            const float f = qq0 + i < Lq ? p.scale : 0.f;  // rows past the request add zero
-            uint8_t* stage = S.dq_stage[ch];
+        // The dQ tile of step tt (its GEMMs complete) leaves through shared memory:
+        // this lane's query row, 32 columns (half ch), is loaded from TMEM while the
+        // step's P / dS are stored, then staged; warp 2 adds the staged tile to the
+        // fp32 accumulator with TMA bulk reduce-adds.  dS carries the softmax scale,
+        // so the values go out as they are.
+        uint32_t* const stage_row = reinterpret_cast<uint32_t*>(S.dq_stage[ch] + i * 128);
+        auto stage_dq = [&](const uint32_t (&u)[32]) {
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(smem_u32(stage + sw128_off(i, c))),
-                             "f"(__uint_as_float(u[4 * c]) * f), "f"(__uint_as_float(u[4 * c + 1]) * f),
-                             "f"(__uint_as_float(u[4 * c + 2]) * f), "f"(__uint_as_float(u[4 * c + 3]) * f)
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(smem_u32(stage_row) + (((c ^ (i & 7))) << 4)),
+                             "r"(u[4 * c]), "r"(u[4 * c + 1]), "r"(u[4 * c + 2]), "r"(u[4 * c + 3])
                              : "memory");
             }
-            fence_proxy_async_smem();
-            mbar_arrive(&S.dq_staged);  // warp 2 adds the staged tile to the accumulator
-            return true;
         };
         // LSE and D of this lane's query row for head g of the group and query tile
         // qt (+inf / 0 past the request's end and past the last step)
@@ -352,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
 
         // step t = g_c * nqt + qt_c (head g_c of the group, query tile qt_c)
-        int g_c = 0, qt_c = 0, q0_prev = 0;
+        int g_c = 0, qt_c = 0;
         float lse_cur, d_cur;
         load_row(0, 0, lse_cur, d_cur);
         for (int t = 0; t < T; ++t) {
@@ -382,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int c_win = W > 0 ? qpos + 1 - W - j0 : 0;
             const float nl2 = -lse_cur * ATTN_LOG2E;  // -inf past the end: P = 0 there
             const uint64_t nl2x2 = f2_pack(nl2, nl2);
-            const uint64_t ndx2 = f2_pack(-d_cur, -d_cur);
+            const uint64_t ndx2 = f2_pack(-d_cur * p.scale, -d_cur * p.scale);
             uint32_t pw[32], dw[32];  // packed bf16 P and dS of this query row, 64 key columns
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
@@ -396,18 +387,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(&S.sdp_free);
                 }
                 if (full)
-                    p_ds_half<false>(sr, dr, col, sc2, nl2x2, ndx2, c_last, c_first_end, c_win, pw + half * 16,
-                                     dw + half * 16);
+                    p_ds_half<false>(sr, dr, col, sc2, nl2x2, scx2, ndx2, c_last, c_first_end, c_win,
+                                     pw + half * 16, dw + half * 16);
                 else
-                    p_ds_half<true>(sr, dr, col, sc2, nl2x2, ndx2, c_last, c_first_end, c_win, pw + half * 16,
-                                    dw + half * 16);
+                    p_ds_half<true>(sr, dr, col, sc2, nl2x2, scx2, ndx2, c_last, c_first_end, c_win,
+                                    pw + half * 16, dw + half * 16);
             }
+            uint32_t u[32];  // dQ of step t - 1
             if (t > 0) {  // the previous step's GEMMs must be done reading P / dS
                 ok = mbar_wait(&S.mma2_done, (t - 1) & 1, abort);
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
                     break;
                 }
+                tc_fence_after();
+                tmem_ld32(tmem + lane_base + cDQ + ((t - 1) & 1) * D + ch * 32, u);
             }
             // 64 key columns = atom ch, chunks 0..7 of 16 bytes
 #pragma unroll
@@ -424,25 +418,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(&S.pds_full);
             if (t > 0) {
-                tc_fence_after();
-                if (!__all_sync(0xffffffffu, flush_dq(t - 1, q0_prev))) {
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(&S.dq_free[(t - 1) & 1]);
+                // the bulk reduce of step t - 2 has finished reading the stage
+                ok = t == 1 || mbar_wait(&S.dq_stage_free, (t - 2) & 1, abort);
+                if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
                     break;
                 }
+                stage_dq(u);
+                fence_proxy_async_smem();
+                mbar_arrive(&S.dq_staged);
             }
             lse_cur = lse_nxt;
             d_cur = d_nxt;
-            q0_prev = q0;
             g_c = g_n;
             qt_c = qt_n;
         }
         // last step's dQ, then dK (column half 0) / dV (column half 1)
         if (ok && T > 0) {
-            ok = mbar_wait(&S.mma2_done, (T - 1) & 1, abort);
-            ok = __all_sync(0xffffffffu, ok);
+            ok = __all_sync(0xffffffffu, mbar_wait(&S.mma2_done, (T - 1) & 1, abort));
             if (ok) {
                 tc_fence_after();
-                ok = __all_sync(0xffffffffu, flush_dq(T - 1, q0_prev));
+                uint32_t u[32];
+                tmem_ld32(tmem + lane_base + cDQ + ((T - 1) & 1) * D + ch * 32, u);
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(&S.dq_free[(T - 1) & 1]);
+                ok = __all_sync(0xffffffffu, T == 1 || mbar_wait(&S.dq_stage_free, (T - 2) & 1, abort));
+                if (ok) {
+                    stage_dq(u);
+                    fence_proxy_async_smem();
+                    mbar_arrive(&S.dq_staged);
+                }
             }
         }
         if (ok && T > 0) ok = mbar_wait(&S.final_bar, 0, abort);
@@ -452,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kpos = j0 + i;
         const size_t rowoff = ((size_t)(k_start + kpos) * p.hkv + kvh) * D;
         const uint32_t col = ch == 0 ? cDK : cDV;
-        const float f = ch == 0 ? p.scale : 1.f;
+        const float f = 1.f;  // dK: the scale rides on dS
         __nv_bfloat16* outp = ch == 0 ? p.dk : p.dv;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
