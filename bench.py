@@ -39,10 +39,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel source it was measured on and is reported only while that source is
 # unchanged.
 NCU_TRAFFIC = {
-    # profiles/fwd_kernel_extend_varlen.md: 443.2 MB read + 259.3 MB written per launch
-    "fwd_kernel/extend_varlen": {"src": "df9fc773b52a7b4f", "bytes": 702_425_600},
-    # profiles/bwd_main_kernel_train.md: 2.291 GB read + 1.026 GB written per launch
-    "bwd_main_kernel/train": {"src": "c56ba150c8eb65bb", "bytes": 3_317_215_000},
+    # profiles/fwd_kernel_extend_varlen.md: 444.4 MB read + 259.2 MB written per launch
+    "fwd_kernel/extend_varlen": {"src": "d72806b19cb54231", "bytes": 703_589_376},
+    # profiles/bwd_main_kernel_train.md: 2.549 GB read + 1.126 GB written per launch
+    "bwd_main_kernel/train": {"src": "e7c5b15167ee58ec", "bytes": 3_675_104_000},
     # profiles/decode_split_kernel_decode_sink.md: decode_split_kernel, 1.943 GB + 0.033 GB
     "decode/decode_sink": {"src": "02720d9c34caae7c", "bytes": 1_976_352_288},
     # profiles/decode_split_kernel_decode_window.md: decode_split_kernel, 1.074 GB + 0.011 GB
