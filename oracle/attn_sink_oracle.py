@@ -272,6 +272,71 @@ def attn_decode_paged(q, k_cache, v_cache, page_table, seqlens, page_size, sink=
 
 
 # ---------------------------------------------------------------------------
+# Paged cache writes and paged extend
+
+def paged_slot(page_table, b: int, t: int, page_size: int) -> int:
+    """Physical slot of logical token ``t`` of request ``b`` (the page-table
+    indirection of the sglang attention-sink PR's suggested code)."""
+    return int(page_table[b, t // page_size]) * page_size + t % page_size
+
+
+def kv_append(k_cache, v_cache, page_table, seqlens, k_new, v_new, page_size, cu_new=None):
+    """Writes each request's new K/V rows into its pages and returns the new caches.
+
+    Request ``b`` has ``n_b`` new rows (``cu_new[b+1] - cu_new[b]``; one row,
+    row ``b`` of ``k_new``, when ``cu_new`` is None) and ``seqlens[b]`` counts
+    them: they are logical tokens ``L_b - n_b .. L_b - 1``, written in order.
+    This is the cache update that precedes attention in KV-cache decode
+    (flash-attention PR "feat: Implement Sink Attention", Description: the
+    KV-cache decode path with a sink).  Caches are torch tensors
+    (num_pages, page_size, Hkv, d); copies are exact.
+    """
+    import torch
+    kc = k_cache.clone()
+    vc = v_cache.clone()
+    kflat = kc.view(-1, *kc.shape[2:])
+    vflat = vc.view(-1, *vc.shape[2:])
+    L = _ints(seqlens)
+    pt = _ints(page_table)
+    B = len(L)
+    cn = np.arange(B + 1) if cu_new is None else _ints(cu_new)
+    for b in range(B):
+        n = int(cn[b + 1] - cn[b])
+        for r in range(n):
+            t = int(L[b]) - n + r
+            slot = paged_slot(pt, b, t, page_size)
+            kflat[slot] = k_new[int(cn[b]) + r]
+            vflat[slot] = v_new[int(cn[b]) + r]
+    return kc, vc
+
+
+def gather_paged(cache, page_table, seqlens, page_size):
+    """Contiguous (sum L_b, Hkv, d) copy of each request's tokens 0..L_b-1 and
+    the matching cu_seqlens (B+1)."""
+    import torch
+    flat = cache.reshape(-1, *cache.shape[2:])
+    L = _ints(seqlens)
+    pt = _ints(page_table)
+    idx = [paged_slot(pt, b, t, page_size) for b in range(len(L)) for t in range(int(L[b]))]
+    cu = np.zeros(len(L) + 1, dtype=np.int64)
+    cu[1:] = np.cumsum(L)
+    return flat[torch.as_tensor(idx, dtype=torch.long)], cu
+
+
+def attn_fwd_paged(q, k_cache, v_cache, page_table, seqlens_k, cu_seqlens_q, page_size, sink,
+                   win_first=0, win_last=0, causal=True, scale=0.0, heads=None, requests=None,
+                   rows=None):
+    """Varlen extend / prefill whose keys and values live in a paged cache:
+    request ``b``'s query rows (``cu_seqlens_q``) are the last ``Lq_b`` of its
+    ``seqlens_k[b]`` cached tokens (bottom-right causal alignment), read through
+    the page table.  The same attention as ``attn_fwd`` on the gathered tokens."""
+    K, cu_k = gather_paged(k_cache, page_table, seqlens_k, page_size)
+    V, _ = gather_paged(v_cache, page_table, seqlens_k, page_size)
+    return attn_fwd(q, K, V, sink, cu_seqlens_q, cu_k, win_first, win_last, causal, scale,
+                    heads=heads, requests=requests, rows=rows)
+
+
+# ---------------------------------------------------------------------------
 # Backward
 
 def attn_bwd(q, k, v, sink, dout, cu_seqlens_q, cu_seqlens_k, win_first=0, win_last=0,

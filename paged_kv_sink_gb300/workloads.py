@@ -21,9 +21,14 @@ Workloads (shapes from the two forms of the sink described on the pages):
   d 128, page 64, L U{8192..65536}.
 * ``train``          -- training forward+backward with sink: B 2, L 8192,
   Hq 64, Hkv 8, d 64, sink ~ N(0,1), dO ~ N(0,1).
+* ``extend_paged``   -- the ``extend_varlen`` shapes with each request's
+  prefix in a paged cache (page 16, random page permutation; the serving
+  extend path reads its prefix through the page table, sglang PR "To implement
+  attention-sink", suggested code) and the chunk's K/V appended by the call.
 
 Recipe: one ``torch.Generator('cpu')`` seeded with ``seed``; draws are taken in
-the fixed order lengths -> page permutation -> q -> k -> v -> sink -> dO.
+the fixed order lengths -> page permutation -> q -> k -> v -> sink -> dO (for
+the paged extend: q -> K cache -> V cache -> new K -> new V -> sink).
 Integer "uniform a-b" ranges include both ends.  Floating inputs are drawn in
 fp32 and rounded to bf16 (round-to-nearest-even, torch's conversion).
 """
@@ -137,6 +142,55 @@ class Decode:
         return self.scale if self.scale > 0 else 1.0 / math.sqrt(self.head_dim)
 
 
+@dataclass
+class PagedExtend:
+    """Varlen extend against a paged KV cache (all CPU tensors).
+
+    Request ``b`` has ``seqlens_k[b]`` tokens in the cache: a prefix followed by
+    its new chunk of ``Lq_b`` tokens (the query rows, ``cu_seqlens_q``).  The
+    chunk's K/V rows are ``k_new``/``v_new``; the cache slots of the chunk hold
+    unrelated values until the chunk is appended."""
+    name: str
+    q: torch.Tensor            # (total_q, hq, d) bf16
+    k_new: torch.Tensor        # (total_q, hkv, d) bf16
+    v_new: torch.Tensor        # (total_q, hkv, d) bf16
+    k_cache: torch.Tensor      # (num_pages, page_size, hkv, d) bf16
+    v_cache: torch.Tensor
+    page_table: torch.Tensor   # (B, max_pages) int32
+    seqlens_k: torch.Tensor    # (B,) int32, prefix + chunk
+    cu_seqlens_q: torch.Tensor  # (B+1,) int32
+    page_size: int
+    sink: Optional[torch.Tensor]
+    win_first: int = 0
+    win_last: int = 0
+    causal: bool = True
+    scale: float = 0.0
+
+    @property
+    def batch(self) -> int:
+        return self.cu_seqlens_q.numel() - 1
+
+    @property
+    def hq(self) -> int:
+        return self.q.shape[1]
+
+    @property
+    def hkv(self) -> int:
+        return self.k_cache.shape[2]
+
+    @property
+    def seqlens_q(self):
+        return (self.cu_seqlens_q[1:] - self.cu_seqlens_q[:-1]).tolist()
+
+    @property
+    def max_seqlen_q(self) -> int:
+        return max(self.seqlens_q) if self.batch else 0
+
+    @property
+    def max_seqlen_k(self) -> int:
+        return int(self.seqlens_k.max()) if self.batch else 0
+
+
 def _randint(g, lo, hi, n):
     """n integers uniform on [lo, hi] (both ends included)."""
     return torch.randint(lo, hi + 1, (n,), generator=g, dtype=torch.int64)
@@ -222,6 +276,45 @@ def make_decode(*, name="decode", seqlens, hq, hkv, d, page_size, sink=("uniform
                   sink=s, win_first=win_first, win_last=win_last, scale=scale)
 
 
+def make_paged_extend(*, name="paged_extend", seqlens_q, seqlens_k, hq, hkv, d, page_size,
+                      sink=(-2.0, 4.0), win_first=0, win_last=0, causal=True, scale=0.0, seed=0,
+                      g=None, extra_pages=0) -> PagedExtend:
+    """Build a paged varlen extend problem.
+
+    Lengths (lists or a callable ``g -> (seqlens_q, seqlens_k)``) are drawn
+    first, then the page permutation (as in ``make_decode``), then q, the two
+    caches, the chunk's new K and V, and the sink."""
+    if g is None:
+        g = torch.Generator().manual_seed(seed)
+    if callable(seqlens_q):
+        seqlens_q, seqlens_k = seqlens_q(g)
+    seqlens_q = [int(x) for x in seqlens_q]
+    seqlens_k = [int(x) for x in seqlens_k]
+    B = len(seqlens_q)
+    npages = [(L + page_size - 1) // page_size for L in seqlens_k]
+    pool = max(sum(npages) + extra_pages, 1)
+    perm = torch.randperm(pool, generator=g).to(torch.int32)
+    max_pages = max(max(npages) if B else 0, 1)
+    pt = torch.full((B, max_pages), -1, dtype=torch.int32)
+    off = 0
+    for b, n in enumerate(npages):
+        pt[b, :n] = perm[off:off + n]
+        off += n
+    cu_q = torch.zeros(B + 1, dtype=torch.int32)
+    cu_q[1:] = torch.tensor(seqlens_q, dtype=torch.int64).cumsum(0).to(torch.int32)
+    tq = int(cu_q[-1])
+    q = _normal_bf16(g, (tq, hq, d))
+    kc = _normal_bf16(g, (pool, page_size, hkv, d))
+    vc = _normal_bf16(g, (pool, page_size, hkv, d))
+    kn = _normal_bf16(g, (tq, hkv, d))
+    vn = _normal_bf16(g, (tq, hkv, d))
+    s = _sink(g, sink, hq)
+    return PagedExtend(name=name, q=q, k_new=kn, v_new=vn, k_cache=kc, v_cache=vc, page_table=pt,
+                       seqlens_k=torch.tensor(seqlens_k, dtype=torch.int32), cu_seqlens_q=cu_q,
+                       page_size=page_size, sink=s, win_first=win_first, win_last=win_last,
+                       causal=causal, scale=scale)
+
+
 # ---------------------------------------------------------------------------
 # The five named workloads.
 
@@ -253,6 +346,18 @@ def decode_window(seed=0):
                        win_first=1024, win_last=7168, seed=seed)
 
 
+def extend_paged(seed=0, n_req=8, page_size=16):
+    """The varlen-extend shapes with the prefix in a paged cache (page size 16,
+    random page permutation) and the chunk appended by the call."""
+    def lens(g):
+        prefix = _randint(g, 0, 16384, n_req)
+        chunk = _randint(g, 512, 8192, n_req)
+        return chunk.tolist(), (prefix + chunk).tolist()
+    return make_paged_extend(name=f"extend_paged 8req prefix U0-16384 chunk U512-8192 Hq64 Hkv8 d64 ps{page_size} sink",
+                             seqlens_q=lens, seqlens_k=None, hq=64, hkv=8, d=64, page_size=page_size,
+                             sink=(-2.0, 4.0), seed=seed)
+
+
 def train(seed=0):
     return make_prefill(name="train B2 L8192 Hq64 Hkv8 d64 causal sink fwd+bwd",
                         seqlens_q=[8192, 8192], hq=64, hkv=8, d=64, sink="normal",
@@ -265,6 +370,7 @@ WORKLOADS = {
     "decode_sink": decode_sink,
     "decode_window": decode_window,
     "train": train,
+    "extend_paged": extend_paged,
 }
 
 
