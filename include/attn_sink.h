@@ -165,6 +165,79 @@ int attn_sink_decode_paged_noalloc(const attn_bf16* q, const attn_bf16* k_cache,
                                    attn_bf16* out, float* lse, void* stream);
 
 /*
+ * Writes new tokens' K/V rows into a paged cache (the cache update that
+ * precedes attention in KV-cache decode: flash-attention PR "feat: Implement
+ * Sink Attention", Description; a request's tokens are reached through its
+ * page-table row: sglang PR "To implement attention-sink", suggested code).
+ *
+ *   k_new, v_new   (rows, hkv, head_dim) bf16; request b's new rows are
+ *                  [cu_new[b], cu_new[b+1]), or row b alone when cu_new is NULL
+ *   cu_new         (batch+1,) int32 device or NULL (then max_new must be 1)
+ *   seqlens        (batch,) int32 device: cache length INCLUDING the new rows,
+ *                  so request b's n_b new rows become its logical tokens
+ *                  seqlens[b] - n_b .. seqlens[b] - 1
+ *   page_table     (batch, max_pages) int32 device, as in attn_sink_decode_paged
+ *   max_new        host upper bound of n_b (sizes the grid)
+ *   k_cache, v_cache   (num_pages, page_size, hkv, head_dim) bf16, written in place
+ * A row whose slot would fall outside the cache (page id outside
+ * [0, num_pages), or more new rows than cached tokens) is skipped and sets
+ * ATTN_SINK_DEV_PAGE_OOB / ATTN_SINK_DEV_SEQLEN_OOB.  Rows of different
+ * requests must not share a slot (the write order between them is undefined).
+ * Supported: head_dim 64 or 128.
+ */
+int attn_sink_kv_append(const attn_bf16* k_new, const attn_bf16* v_new, const int32_t* cu_new,
+                        const int32_t* seqlens, const int32_t* page_table, int max_pages, int batch,
+                        int hkv, int head_dim, int page_size, int num_pages, int max_new,
+                        attn_bf16* k_cache, attn_bf16* v_cache, void* stream);
+
+/*
+ * Paged decode with the new token's K/V appended in the same call: writes
+ * k_new[b], v_new[b] ((batch, hkv, head_dim) bf16) at logical token
+ * seqlens[b] - 1 of each request, then runs attn_sink_decode_paged on the
+ * updated caches (KV-cache decode with a sink: flash-attention PR "feat:
+ * Implement Sink Attention", Description).  Every other argument as in
+ * attn_sink_decode_paged; k_cache / v_cache are written.  The call makes no
+ * host synchronisation and depends only on its arguments, so it can be
+ * captured in a CUDA graph (its scratch comes from a stream-ordered pool).
+ */
+int attn_sink_decode_paged_append(const attn_bf16* q, const attn_bf16* k_new, const attn_bf16* v_new,
+                                  attn_bf16* k_cache, attn_bf16* v_cache, const int32_t* page_table,
+                                  int max_pages, const int32_t* seqlens, int batch, int hq, int hkv,
+                                  int head_dim, int page_size, int num_pages, const float* sink,
+                                  int win_first, int win_last, float scale, attn_bf16* out,
+                                  float* lse, void* stream);
+
+/*
+ * Varlen extend / prefill whose keys and values live in a paged cache (the
+ * serving extend path: sglang PR "openai oss attention sink support with
+ * trtllm-gen backend", Highlights: the extend path passes sink=; the prefix is
+ * reached through the page table: sglang PR "To implement attention-sink",
+ * suggested code).  Request b's query rows [cu_seqlens_q[b], cu_seqlens_q[b+1])
+ * are the LAST Lq_b of its seqlens_k[b] cached tokens (bottom-right causal
+ * alignment, as in attn_sink_fwd).
+ *
+ *   q            (total_q, hq, 64) bf16
+ *   k_new, v_new (total_q, hkv, 64) bf16, the chunk's own K/V, or both NULL.
+ *                When given they are first appended into the cache at the
+ *                chunk's positions (attn_sink_kv_append with cu_new =
+ *                cu_seqlens_q); when NULL the cache must already hold them.
+ *   k_cache, v_cache  (num_pages, page_size, hkv, 64) bf16
+ *   page_table   (batch, max_pages) int32 device
+ *   seqlens_k    (batch,) int32 device, prefix + chunk
+ *   max_seqlen_q, max_seqlen_k   host upper bounds (grid sizing, append grid)
+ *   sink, win_first, win_last, causal, scale, out, lse: as in attn_sink_fwd
+ * Supported: head_dim 64; hq % hkv == 0; page_size a power of two >= 8
+ * (a 128-key tile is then one TMA copy per page segment).
+ */
+int attn_sink_fwd_paged(const attn_bf16* q, const attn_bf16* k_new, const attn_bf16* v_new,
+                        attn_bf16* k_cache, attn_bf16* v_cache, const int32_t* page_table,
+                        int max_pages, const int32_t* cu_seqlens_q, const int32_t* seqlens_k,
+                        int batch, int total_q, int hq, int hkv, int head_dim, int page_size,
+                        int num_pages, int max_seqlen_q, int max_seqlen_k, const float* sink,
+                        int win_first, int win_last, int causal, float scale, attn_bf16* out,
+                        float* lse, void* stream);
+
+/*
  * Backward of attn_sink_fwd: gradients of sum(dout * out) with respect to q,
  * k, v and the sink.  Page: flash-attention PR "feat: Implement Sink Attention" (Key Changes: the
  * backward pass computes and returns the gradient of the learnable sink).

@@ -31,6 +31,11 @@ _SIGS = {
                                        _P, _P],
     "attn_sink_bwd": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I,
                       _I, _F, _P, _P, _P, _P, _P],
+    "attn_sink_kv_append": [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P],
+    "attn_sink_decode_paged_append": [_P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _I, _I, _F,
+                                      _P, _P, _P],
+    "attn_sink_fwd_paged": [_P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I,
+                            _I, _I, _F, _P, _P, _P],
     "attn_sink_visible_ranges": [_P, _I, _I, _I, _P, _P],
     "attn_sink_visible_slots": [_P, _P, _I, _I, _I, _I, _I, _I, _P, _I, _P],
     "attn_sink_device_status": [_P],
@@ -150,6 +155,75 @@ def attn_sink_decode_paged_noalloc(q, k_cache, v_cache, page_table, seqlens, sin
     return attn_sink_decode_paged(q, k_cache, v_cache, page_table, seqlens, sink, win_first, win_last,
                                   scale, out, lse, return_lse, stream,
                                   _entry="attn_sink_decode_paged_noalloc")
+
+
+def attn_sink_kv_append(k_new, v_new, k_cache, v_cache, page_table, seqlens, cu_new=None,
+                        max_new=None, stream=None):
+    """Writes the new K/V rows into the paged caches in place (see the C header)."""
+    for t, n in ((k_new, "k_new"), (v_new, "v_new"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n)
+    _need(page_table, torch.int32, "page_table")
+    _need(seqlens, torch.int32, "seqlens")
+    _need(cu_new, torch.int32, "cu_new")
+    npages, ps, hkv, d = k_cache.shape
+    B = seqlens.numel()
+    if max_new is None:
+        max_new = 1 if cu_new is None else int((cu_new[1:] - cu_new[:-1]).max()) if B else 0
+    rc = lib().attn_sink_kv_append(_ptr(k_new), _ptr(v_new), _ptr(cu_new), _ptr(seqlens), _ptr(page_table),
+                                   page_table.shape[1], B, hkv, d, ps, npages, int(max_new), _ptr(k_cache),
+                                   _ptr(v_cache), _stream(stream))
+    _check("attn_sink_kv_append", rc)
+    return k_cache, v_cache
+
+
+def attn_sink_decode_paged_append(q, k_new, v_new, k_cache, v_cache, page_table, seqlens, sink=None,
+                                  win_first=0, win_last=0, scale=0.0, out=None, lse=None,
+                                  return_lse=True, stream=None):
+    """Paged decode with the new token's K/V (k_new, v_new: (B, Hkv, d)) written into
+    the caches first, in the same call."""
+    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n)
+    _need(page_table, torch.int32, "page_table")
+    _need(seqlens, torch.int32, "seqlens")
+    _need(sink, torch.float32, "sink")
+    B, hq, d = q.shape
+    npages, ps, hkv, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, hq), dtype=torch.float32, device=q.device)
+    rc = lib().attn_sink_decode_paged_append(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                             _ptr(page_table), page_table.shape[1], _ptr(seqlens), B, hq, hkv, d,
+                                             ps, npages, _ptr(sink), int(win_first), int(win_last), float(scale),
+                                             _ptr(out), _ptr(lse), _stream(stream))
+    _check("attn_sink_decode_paged_append", rc)
+    return out, lse
+
+
+def attn_sink_fwd_paged(q, k_cache, v_cache, page_table, cu_seqlens_q, seqlens_k, max_seqlen_q,
+                        max_seqlen_k, sink=None, k_new=None, v_new=None, win_first=0, win_last=0,
+                        causal=True, scale=0.0, out=None, lse=None, return_lse=True, stream=None):
+    """Varlen extend against a paged K/V cache; with k_new/v_new the chunk's K/V
+    are appended into the cache first.  Returns (out, lse)."""
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (k_new, "k_new"), (v_new, "v_new")):
+        _need(t, torch.bfloat16, n)
+    _need(page_table, torch.int32, "page_table")
+    _need(cu_seqlens_q, torch.int32, "cu_seqlens_q")
+    _need(seqlens_k, torch.int32, "seqlens_k")
+    _need(sink, torch.float32, "sink")
+    tq, hq, d = q.shape
+    npages, ps, hkv, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((hq, tq), dtype=torch.float32, device=q.device)
+    rc = lib().attn_sink_fwd_paged(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                   _ptr(page_table), page_table.shape[1], _ptr(cu_seqlens_q), _ptr(seqlens_k),
+                                   cu_seqlens_q.numel() - 1, tq, hq, hkv, d, ps, npages, int(max_seqlen_q),
+                                   int(max_seqlen_k), _ptr(sink), int(win_first), int(win_last),
+                                   1 if causal else 0, float(scale), _ptr(out), _ptr(lse), _stream(stream))
+    _check("attn_sink_fwd_paged", rc)
+    return out, lse
 
 
 def attn_sink_bwd(q, k, v, sink, out, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,

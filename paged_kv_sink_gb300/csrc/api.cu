@@ -12,6 +12,7 @@
 #include "bwd.h"
 #include "common.cuh"
 #include "decode.h"
+#include "kv_append.h"
 #include "prefill.h"
 
 namespace {
@@ -99,12 +100,13 @@ const char* attn_sink_last_error(void) { return t_last_error.c_str(); }
 
 const char* attn_sink_version(void) { return "attn_sink_gb300 0.1 (sm_103a)"; }
 
-int attn_sink_decode_paged(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_cache,
-                           const int32_t* page_table, int max_pages, const int32_t* seqlens,
-                           int batch, int hq, int hkv, int head_dim, int page_size, int num_pages,
-                           const float* sink, int win_first, int win_last, float scale,
-                           attn_bf16* out, float* lse, void* stream) {
-    t_last_error.clear();
+}  // extern "C"
+
+namespace {
+
+int validate_decode(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_cache,
+                    const int32_t* page_table, int max_pages, const int32_t* seqlens, int batch, int hq,
+                    int hkv, int head_dim, int page_size, int num_pages, int win_first, attn_bf16* out) {
     if (batch < 0 || hq <= 0 || hkv <= 0 || max_pages <= 0 || page_size <= 0 || num_pages <= 0)
         return fail(ATTN_SINK_ERR_INVALID, "decode: sizes must be positive (batch may be 0)");
     if (win_first < 0) return fail(ATTN_SINK_ERR_INVALID, "decode: win_first must be >= 0");
@@ -118,7 +120,13 @@ int attn_sink_decode_paged(const attn_bf16* q, const attn_bf16* k_cache, const a
         return fail(ATTN_SINK_ERR_INVALID, "decode: q, caches and out must be 16-byte aligned");
     if ((long long)num_pages * page_size >= (1LL << 31) || (long long)max_pages * page_size >= (1LL << 31))
         return fail(ATTN_SINK_ERR_UNSUPPORTED, "decode: cache slots must fit in int32");
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return ATTN_SINK_OK;
+}
+
+int run_decode(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_cache, const int32_t* page_table,
+               int max_pages, const int32_t* seqlens, int batch, int hq, int hkv, int head_dim, int page_size,
+               int num_pages, const float* sink, int win_first, int win_last, float scale, attn_bf16* out,
+               float* lse, cudaStream_t s) {
     attn::decode::Args a;
     a.q = q;
     a.k_cache = k_cache;
@@ -148,6 +156,88 @@ int attn_sink_decode_paged(const attn_bf16* q, const attn_bf16* k_cache, const a
     e = attn::decode::launch(a, pl, part_o, part_ml, s);
     if (e != cudaSuccess) return cuda_fail(e, "decode: launch");
     return ATTN_SINK_OK;
+}
+
+int run_append(const attn_bf16* k_new, const attn_bf16* v_new, const int32_t* cu_new, const int32_t* seqlens,
+               const int32_t* page_table, int max_pages, int batch, int hkv, int head_dim, int page_size,
+               int num_pages, int max_new, attn_bf16* k_cache, attn_bf16* v_cache, cudaStream_t s) {
+    attn::kvappend::Args a;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.cu_new = cu_new;
+    a.seqlens = seqlens;
+    a.page_table = page_table;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.max_pages = max_pages;
+    a.batch = batch;
+    a.hkv = hkv;
+    a.head_dim = head_dim;
+    a.page_size = page_size;
+    a.num_pages = num_pages;
+    a.max_new = max_new;
+    cudaError_t e = attn::kvappend::launch(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "kv_append: launch");
+    return ATTN_SINK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_sink_decode_paged(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_cache,
+                           const int32_t* page_table, int max_pages, const int32_t* seqlens,
+                           int batch, int hq, int hkv, int head_dim, int page_size, int num_pages,
+                           const float* sink, int win_first, int win_last, float scale,
+                           attn_bf16* out, float* lse, void* stream) {
+    t_last_error.clear();
+    int rc = validate_decode(q, k_cache, v_cache, page_table, max_pages, seqlens, batch, hq, hkv, head_dim,
+                             page_size, num_pages, win_first, out);
+    if (rc != ATTN_SINK_OK || batch == 0) return rc;
+    return run_decode(q, k_cache, v_cache, page_table, max_pages, seqlens, batch, hq, hkv, head_dim, page_size,
+                      num_pages, sink, win_first, win_last, scale, out, lse, static_cast<cudaStream_t>(stream));
+}
+
+int attn_sink_kv_append(const attn_bf16* k_new, const attn_bf16* v_new, const int32_t* cu_new,
+                        const int32_t* seqlens, const int32_t* page_table, int max_pages, int batch, int hkv,
+                        int head_dim, int page_size, int num_pages, int max_new, attn_bf16* k_cache,
+                        attn_bf16* v_cache, void* stream) {
+    t_last_error.clear();
+    if (batch < 0 || hkv <= 0 || max_pages <= 0 || page_size <= 0 || num_pages <= 0 || max_new < 0)
+        return fail(ATTN_SINK_ERR_INVALID, "kv_append: sizes must be positive (batch, max_new may be 0)");
+    if (head_dim != 64 && head_dim != 128)
+        return fail(ATTN_SINK_ERR_UNSUPPORTED, "kv_append: head_dim %d not supported (64, 128)", head_dim);
+    if ((long long)num_pages * page_size >= (1LL << 31) || (long long)max_pages * page_size >= (1LL << 31))
+        return fail(ATTN_SINK_ERR_UNSUPPORTED, "kv_append: cache slots must fit in int32");
+    if (batch == 0 || max_new == 0) return ATTN_SINK_OK;
+    if (!k_new || !v_new || !seqlens || !page_table || !k_cache || !v_cache)
+        return fail(ATTN_SINK_ERR_INVALID, "kv_append: NULL tensor pointer");
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+        return fail(ATTN_SINK_ERR_INVALID, "kv_append: tensors must be 16-byte aligned");
+    if (!cu_new && max_new != 1)
+        return fail(ATTN_SINK_ERR_INVALID, "kv_append: without cu_new every request appends one row (max_new 1)");
+    return run_append(k_new, v_new, cu_new, seqlens, page_table, max_pages, batch, hkv, head_dim, page_size,
+                      num_pages, max_new, k_cache, v_cache, static_cast<cudaStream_t>(stream));
+}
+
+int attn_sink_decode_paged_append(const attn_bf16* q, const attn_bf16* k_new, const attn_bf16* v_new,
+                                  attn_bf16* k_cache, attn_bf16* v_cache, const int32_t* page_table,
+                                  int max_pages, const int32_t* seqlens, int batch, int hq, int hkv, int head_dim,
+                                  int page_size, int num_pages, const float* sink, int win_first, int win_last,
+                                  float scale, attn_bf16* out, float* lse, void* stream) {
+    t_last_error.clear();
+    int rc = validate_decode(q, k_cache, v_cache, page_table, max_pages, seqlens, batch, hq, hkv, head_dim,
+                             page_size, num_pages, win_first, out);
+    if (rc != ATTN_SINK_OK || batch == 0) return rc;
+    if (!k_new || !v_new) return fail(ATTN_SINK_ERR_INVALID, "decode_append: NULL k_new / v_new");
+    if (!aligned16(k_new) || !aligned16(v_new))
+        return fail(ATTN_SINK_ERR_INVALID, "decode_append: k_new, v_new must be 16-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    rc = run_append(k_new, v_new, nullptr, seqlens, page_table, max_pages, batch, hkv, head_dim, page_size,
+                    num_pages, 1, k_cache, v_cache, s);
+    if (rc != ATTN_SINK_OK) return rc;
+    return run_decode(q, k_cache, v_cache, page_table, max_pages, seqlens, batch, hq, hkv, head_dim, page_size,
+                      num_pages, sink, win_first, win_last, scale, out, lse, s);
 }
 
 int attn_sink_visible_ranges(const int32_t* seqlens, int batch, int win_first, int win_last,
@@ -236,6 +326,72 @@ int attn_sink_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, co
     return ATTN_SINK_OK;
 }
 
+int attn_sink_fwd_paged(const attn_bf16* q, const attn_bf16* k_new, const attn_bf16* v_new, attn_bf16* k_cache,
+                        attn_bf16* v_cache, const int32_t* page_table, int max_pages,
+                        const int32_t* cu_seqlens_q, const int32_t* seqlens_k, int batch, int total_q, int hq,
+                        int hkv, int head_dim, int page_size, int num_pages, int max_seqlen_q, int max_seqlen_k,
+                        const float* sink, int win_first, int win_last, int causal, float scale,
+                        attn_bf16* out, float* lse, void* stream) {
+    t_last_error.clear();
+    if (batch < 0 || total_q < 0 || hq <= 0 || hkv <= 0 || max_pages <= 0 || page_size <= 0 || num_pages <= 0 ||
+        max_seqlen_q < 0 || max_seqlen_k < 0 || win_first < 0)
+        return fail(ATTN_SINK_ERR_INVALID, "fwd_paged: sizes must be non-negative (heads, pages positive)");
+    if (win_last > 0 && !causal)
+        return fail(ATTN_SINK_ERR_INVALID, "fwd_paged: first/last-window selection needs causal attention");
+    if (head_dim != 64)
+        return fail(ATTN_SINK_ERR_UNSUPPORTED, "fwd_paged: head_dim %d not supported (64)", head_dim);
+    if (hq % hkv) return fail(ATTN_SINK_ERR_UNSUPPORTED, "fwd_paged: hq %% hkv != 0");
+    if (page_size < 8 || (page_size & (page_size - 1)))
+        return fail(ATTN_SINK_ERR_UNSUPPORTED, "fwd_paged: page_size %d not supported (a power of two >= 8)",
+                    page_size);
+    if ((long long)num_pages * page_size >= (1LL << 31) || (long long)max_pages * page_size >= (1LL << 31))
+        return fail(ATTN_SINK_ERR_UNSUPPORTED, "fwd_paged: cache slots must fit in int32");
+    if ((k_new == nullptr) != (v_new == nullptr))
+        return fail(ATTN_SINK_ERR_INVALID, "fwd_paged: k_new and v_new are given together or not at all");
+    if (batch == 0 || total_q == 0 || max_seqlen_q == 0) return ATTN_SINK_OK;
+    if (!q || !k_cache || !v_cache || !page_table || !cu_seqlens_q || !seqlens_k || !out)
+        return fail(ATTN_SINK_ERR_INVALID, "fwd_paged: NULL tensor pointer");
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+        (k_new && (!aligned16(k_new) || !aligned16(v_new))))
+        return fail(ATTN_SINK_ERR_INVALID, "fwd_paged: tensors must be 16-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (k_new) {
+        int rc = run_append(k_new, v_new, cu_seqlens_q, seqlens_k, page_table, max_pages, batch, hkv, head_dim,
+                            page_size, num_pages, max_seqlen_q, k_cache, v_cache, s);
+        if (rc != ATTN_SINK_OK) return rc;
+    }
+    attn::prefill::FwdArgs a = {};
+    a.q = q;
+    a.k = k_cache;
+    a.v = v_cache;
+    a.sink = sink;
+    a.cu_q = cu_seqlens_q;
+    a.cu_k = nullptr;
+    a.out = out;
+    a.lse = lse;
+    a.batch = batch;
+    a.total_q = total_q;
+    a.total_k = 0;
+    a.hq = hq;
+    a.hkv = hkv;
+    a.head_dim = head_dim;
+    a.max_seqlen_q = max_seqlen_q;
+    a.max_seqlen_k = max_seqlen_k;
+    a.win_first = win_first;
+    a.win_last = win_last;
+    a.causal = causal ? 1 : 0;
+    a.scale = resolve_scale(scale, head_dim);
+    a.page_table = page_table;
+    a.seqlens_k = seqlens_k;
+    a.max_pages = max_pages;
+    a.page_size = page_size;
+    a.num_pages = num_pages;
+    std::string err;
+    cudaError_t e = attn::prefill::launch_fwd(a, s, &err);
+    if (e != cudaSuccess) return fail(ATTN_SINK_ERR_CUDA, "fwd_paged: %s: %s", err.c_str(), cudaGetErrorString(e));
+    return ATTN_SINK_OK;
+}
+
 int attn_sink_bwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, const float* sink,
                   const attn_bf16* out, const float* lse, const attn_bf16* dout,
                   const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch, int total_q,
@@ -296,6 +452,7 @@ int attn_sink_device_status(void* stream) {
     int e = attn::decode::status_exchange(s, &bits);
     if (!e) e = attn::prefill::status_exchange(s, &bits);
     if (!e) e = attn::bwd::status_exchange(s, &bits);
+    if (!e) e = attn::kvappend::status_exchange(s, &bits);
     if (e) return cuda_fail(static_cast<cudaError_t>(e), "device_status");
     return bits;
 }

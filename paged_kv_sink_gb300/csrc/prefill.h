@@ -21,6 +21,12 @@ struct FwdArgs {
     float* lse;
     int batch, total_q, total_k, hq, hkv, head_dim, max_seqlen_q, max_seqlen_k, win_first, win_last, causal;
     float scale;
+    // Paged K/V (page_table != nullptr): k / v are the caches (num_pages, page_size,
+    // hkv, d), request b's keys are its first seqlens_k[b] cached tokens and cu_k /
+    // total_k are unused.  page_size is a power of two >= 8.
+    const int32_t* page_table = nullptr;
+    const int32_t* seqlens_k = nullptr;
+    int max_pages = 0, page_size = 0, num_pages = 0;
 };
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s, std::string* what);

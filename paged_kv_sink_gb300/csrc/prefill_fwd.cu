@@ -79,6 +79,12 @@ struct Params {
     int hq, group, n_rt, total_q, total_k;
     int win_first, win_last, causal;
     float scale_log2;
+    // Paged K/V (page_table != nullptr): keys of request b are its first
+    // seqlens_k[b] cache tokens; token t sits at slot
+    // page_table[b][t >> page_shift] << page_shift | (t & (page_size - 1)).
+    const int32_t* page_table;
+    const int32_t* seqlens_k;
+    int max_pages, page_shift, seg_shift, num_pages;  // a tile is 128 >> seg_shift page segments
 };
 
 // Waits that ignore the abort flag (used only to drain work already in flight
@@ -104,12 +110,14 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     const int q_start = p.cu_q[b];
     int Lq = p.cu_q[b + 1] - q_start;
-    const int k_start = p.cu_k[b];
-    int Lk = p.cu_k[b + 1] - k_start;
-    if (q_start + Lq > p.total_q || k_start + Lk > p.total_k || Lq < 0 || Lk < 0) {
+    const bool paged = p.page_table != nullptr;
+    const int k_start = paged ? 0 : p.cu_k[b];
+    int Lk = paged ? p.seqlens_k[b] : p.cu_k[b + 1] - k_start;
+    const long long k_cap = paged ? ((long long)p.max_pages << p.page_shift) : (long long)p.total_k - k_start;
+    if (q_start + Lq > p.total_q || Lk > k_cap || Lq < 0 || Lk < 0) {
         if (threadIdx.x == 0 && rt == 0 && h == 0) raise_status(ATTN_SINK_DEV_SEQLEN_OOB);
         Lq = max(0, min(Lq, p.total_q - q_start));
-        Lk = max(0, min(Lk, p.total_k - k_start));
+        Lk = (int)max(0LL, min((long long)Lk, k_cap));
     }
     const int qs = rt * BM;
     if (qs >= Lq) return;
@@ -163,34 +171,67 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (warp < 4) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtrl));
-        if ((warp == 0 || warp == 2) && lane == 0) {
+        if (warp == 0 || warp == 2) {
             // -------------------------------------------------------- producers
+            // The warp runs the loop converged: lane 0 waits and issues the TMA
+            // copies; with a paged cache lane i first resolves the physical slot
+            // of the tile's i-th page segment.
             const bool is_k = warp == 0;
             const int nst = is_k ? KSTAGE : VSTAGE;
             uint64_t* full = is_k ? S.k_full : S.v_full;
             uint64_t* empty = is_k ? S.k_empty : S.v_empty;
             uint8_t* dst0 = is_k ? S.k[0] : S.v[0];
             const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
-            prefetch_tmap(tm);
-            if (is_k) {
-                prefetch_tmap(&tm_q);
-                mbar_expect_tx(&S.q_full, kTile);
-                tma_load_3d(S.q, &tm_q, &S.q_full, 0, h, q_start + qs);
+            const int nseg = BN >> p.seg_shift;
+            if (lane == 0) {
+                prefetch_tmap(tm);
+                if (is_k) {
+                    prefetch_tmap(&tm_q);
+                    mbar_expect_tx(&S.q_full, kTile);
+                    tma_load_3d(S.q, &tm_q, &S.q_full, 0, h, q_start + qs);
+                }
             }
             int it = 0;
             for (; it < ntiles; ++it) {
                 const int st = it % nst;
-                if (it >= nst && !mbar_wait(&empty[st], ((it / nst) - 1) & 1, abort)) break;
+                if (it >= nst && !__all_sync(0xffffffffu, mbar_wait(&empty[st], ((it / nst) - 1) & 1, abort)))
+                    break;
                 const int t = it < ta ? it : tb + (it - ta);
-                mbar_expect_tx(&full[st], kTile);
-                tma_load_3d(dst0 + st * kTile, tm, &full[st], 0, kvh, k_start + t * BN);
+                if (!paged) {
+                    if (lane == 0) {
+                        mbar_expect_tx(&full[st], kTile);
+                        tma_load_3d(dst0 + st * kTile, tm, &full[st], 0, kvh, k_start + t * BN);
+                    }
+                } else {
+                    // Segment `lane` covers keys j .. j + (1 << seg_shift) - 1, inside one page.
+                    // Keys past the request's end (masked later) read slot 0.
+                    int slot = 0;
+                    const int j = t * BN + (lane << p.seg_shift);
+                    if (lane < nseg && j < Lk) {
+                        const int pg = __ldg(p.page_table + (size_t)b * p.max_pages + (j >> p.page_shift));
+                        if (pg >= 0 && pg < p.num_pages)
+                            slot = (pg << p.page_shift) | (j & ((1 << p.page_shift) - 1));
+                        else
+                            raise_status(ATTN_SINK_DEV_PAGE_OOB);
+                    }
+                    if (lane == 0) mbar_expect_tx(&full[st], kTile);
+                    for (int sg = 0; sg < nseg; ++sg) {
+                        const int sl = __shfl_sync(0xffffffffu, slot, sg);
+                        if (lane == 0)
+                            tma_load_3d(dst0 + st * kTile + ((uint32_t)sg << p.seg_shift) * 128u, tm, &full[st], 0,
+                                        kvh, sl);
+                    }
+                }
             }
             // Drain: every copy issued must have landed before the CTA exits.
-            if (is_k) drain_wait(&S.q_full, 0);
-            for (int st = 0; st < nst; ++st) {
-                const int n = it > st ? (it - st + nst - 1) / nst : 0;
-                if (n > 0) drain_wait(&full[st], (n - 1) & 1);
+            if (lane == 0) {
+                if (is_k) drain_wait(&S.q_full, 0);
+                for (int st = 0; st < nst; ++st) {
+                    const int n = it > st ? (it - st + nst - 1) / nst : 0;
+                    if (n > 0) drain_wait(&full[st], (n - 1) & 1);
+                }
             }
+            __syncwarp();
         } else if (warp == 1 && ntiles > 0) {
             // -------------------------------------------------------- MMA issuer
             // The whole warp runs the loop converged (every lane waits;
@@ -466,10 +507,23 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s, std::string* what) {
     if (a.total_q == 0) return cudaSuccess;
     CUtensorMap tq, tk, tv;
     cudaError_t e;
+    const bool paged = a.page_table != nullptr;
+    int page_shift = 0, seg_shift = 7;
+    if (paged) {
+        while ((1 << page_shift) < a.page_size) ++page_shift;
+        seg_shift = page_shift < 7 ? page_shift : 7;  // segments of min(page_size, 128) rows
+    }
+    const long long krows = paged ? (long long)a.num_pages * a.page_size : a.total_k;
     if ((e = make_map(&tq, a.q, a.hq, a.total_q, BM, what)) != cudaSuccess) return e;
-    if ((e = make_map(&tk, a.k, a.hkv, a.total_k, BN, what)) != cudaSuccess) return e;
-    if ((e = make_map(&tv, a.v, a.hkv, a.total_k, BN, what)) != cudaSuccess) return e;
+    if ((e = make_map(&tk, a.k, a.hkv, krows, 1 << seg_shift, what)) != cudaSuccess) return e;
+    if ((e = make_map(&tv, a.v, a.hkv, krows, 1 << seg_shift, what)) != cudaSuccess) return e;
     Params p;
+    p.page_table = a.page_table;
+    p.seqlens_k = a.seqlens_k;
+    p.max_pages = a.max_pages;
+    p.page_shift = page_shift;
+    p.seg_shift = seg_shift;
+    p.num_pages = a.num_pages;
     p.sink = a.sink;
     p.cu_q = a.cu_q;
     p.cu_k = a.cu_k;
