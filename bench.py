@@ -326,6 +326,76 @@ def bench_train(torch, ext, dev, p, steps, warmup, flush, peaks, peak_src):
                          "algorithmic_flops_per_launch": bf}}
 
 
+def bench_extend_paged(torch, ext, dev, pe, steps, warmup, flush, peaks, peak_src):
+    """The varlen extend through a page table: each step appends the chunk's K/V
+    into the cache and runs the paged forward (one attn_sink_fwd_paged call).
+    FLOPs as the contiguous extend (4*d per visible pair per query head)."""
+    t = dict(q=pe.q.to(dev), kc=pe.k_cache.to(dev), vc=pe.v_cache.to(dev), pt=pe.page_table.to(dev),
+             cq=pe.cu_seqlens_q.to(dev), sk=pe.seqlens_k.to(dev), sink=pe.sink.to(dev),
+             kn=pe.k_new.to(dev), vn=pe.v_new.to(dev))
+    out = torch.empty_like(t["q"])
+    lse = torch.empty((pe.hq, pe.q.shape[0]), dtype=torch.float32, device=dev)
+
+    def step():
+        ext.attn_sink_fwd_paged(t["q"], t["kc"], t["vc"], t["pt"], t["cq"], t["sk"], pe.max_seqlen_q,
+                                pe.max_seqlen_k, t["sink"], t["kn"], t["vn"], pe.win_first, pe.win_last,
+                                out=out, lse=lse)
+
+    times = time_steps(torch, step, steps, warmup, flush)
+    ms = sum(times) / len(times)
+
+    class _Lens:  # the FLOP count only needs the lengths, windows and head sizes
+        seqlens_q = pe.seqlens_q
+        seqlens_k = pe.seqlens_k.tolist()
+        win_first, win_last, causal = pe.win_first, pe.win_last, pe.causal
+        head_dim, hq = pe.q.shape[2], pe.hq
+
+    flops = fwd_flops(_Lens)
+    tf = flops / (ms * 1e-3) / 1e12
+    del t
+    return {"metric": "attn TFLOP/s", "value": tf, "unit": "TFLOP/s", "ms_per_step": ms,
+            "algorithmic_tflop_per_step": flops / 1e12, "page_size": pe.page_size,
+            "roofline": {"kernel": "attn_sink_fwd_paged call (kv_append_kernel + fwd_kernel, paged loads)",
+                         "bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": tf / peaks["bf16_tflops"], "peak_source": f"bf16 burst, {peak_src}",
+                         "traffic": None, "algorithmic_flops_per_launch": flops}}
+
+
+def bench_decode_append(torch, ext, dev, dc, steps, warmup, flush, peaks, peak_src):
+    """Decode with the new token's K/V appended in the same call, launched
+    eagerly and replayed from a CUDA graph.  Bytes: the visible K/V as in
+    bench_decode (the appended row is one of them)."""
+    g = torch.Generator().manual_seed(1)
+    kn = torch.randn(dc.batch, dc.hkv, dc.head_dim, generator=g).to(torch.bfloat16).to(dev)
+    vn = torch.randn(dc.batch, dc.hkv, dc.head_dim, generator=g).to(torch.bfloat16).to(dev)
+    t = dict(q=dc.q.to(dev), kc=dc.k_cache.to(dev), vc=dc.v_cache.to(dev), pt=dc.page_table.to(dev),
+             sl=dc.seqlens.to(dev), sink=None if dc.sink is None else dc.sink.to(dev))
+    out = torch.empty_like(t["q"])
+    lse = torch.empty((dc.batch, dc.hq), dtype=torch.float32, device=dev)
+
+    def step():
+        ext.attn_sink_decode_paged_append(t["q"], kn, vn, t["kc"], t["vc"], t["pt"], t["sl"], t["sink"],
+                                          dc.win_first, dc.win_last, out=out, lse=lse)
+
+    times = time_steps(torch, step, steps, warmup, flush)
+    ms = sum(times) / len(times)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, capture_error_mode="thread_local"):
+        step()
+    times_g = time_steps(torch, graph.replay, steps, warmup, flush)
+    ms_g = sum(times_g) / len(times_g)
+    nvis = _visible_counts(dc.seqlens.tolist(), dc.win_first, dc.win_last)
+    kv_bytes = sum(nvis) * 2 * dc.hkv * dc.head_dim * 2
+    gbs = kv_bytes / (ms * 1e-3) / 1e9
+    del t
+    return {"metric": "decode KV GB/s", "value": gbs, "unit": "GB/s", "ms_per_step": ms,
+            "graph_replay_ms_per_step": ms_g, "graph_replay_gbs": kv_bytes / (ms_g * 1e-3) / 1e9,
+            "kv_bytes": kv_bytes,
+            "roofline": {"kernel": "attn_sink_decode_paged_append call (kv_append + split + combine)",
+                         "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "peak_source": peak_src, "traffic": None}}
+
+
 # ---------------------------------------------------------------------------
 # CPU baseline (the oracle as it stands, on a bounded sample)
 
@@ -400,7 +470,8 @@ def main():
     ap.add_argument("--workload", default="extend_varlen")
     ap.add_argument("--no-extra", action="store_true", help="skip the decode / training workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
-    ap.add_argument("--only", default=None, choices=["decode_sink", "decode_window", "train"],
+    ap.add_argument("--only", default=None,
+                    choices=["decode_sink", "decode_window", "train", "extend_paged", "decode_append"],
                     help="run one secondary workload alone and print its line (for profiling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -429,9 +500,13 @@ def main():
     flush = _flush_buf(torch, dev)
 
     if args.only:
-        w = wl.workload(args.only, seed=rank)
+        w = wl.workload("decode_sink" if args.only == "decode_append" else args.only, seed=rank)
         if args.only == "train":
             r = bench_train(torch, ext, dev, w, args.steps, args.warmup, flush, peaks, peak_src)
+        elif args.only == "extend_paged":
+            r = bench_extend_paged(torch, ext, dev, w, args.steps, args.warmup, flush, peaks, peak_src)
+        elif args.only == "decode_append":
+            r = bench_decode_append(torch, ext, dev, w, args.steps, args.warmup, flush, peaks, peak_src)
         else:
             r = bench_decode(torch, ext, dev, w, args.steps, args.warmup, flush, peaks, peak_src)
         if rank == 0:
@@ -466,6 +541,14 @@ def main():
         extra["train"] = bench_train(torch, ext, dev, tr, max(3, args.steps // 2), args.warmup, flush, peaks,
                                      peak_src)
         del tr
+        pe = wl.workload("extend_paged", seed=rank)
+        extra["extend_paged"] = bench_extend_paged(torch, ext, dev, pe, max(3, args.steps // 2), args.warmup,
+                                                   flush, peaks, peak_src)
+        del pe
+        dc = wl.workload("decode_sink", seed=rank)
+        extra["decode_sink_append"] = bench_decode_append(torch, ext, dev, dc, args.steps, args.warmup, flush,
+                                                          peaks, peak_src)
+        del dc
 
     line = {
         "metric": "attn TFLOP/s (prefill, fwd+bwd) & decode KV GB/s, % of GB300 roofline",
