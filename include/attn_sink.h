@@ -106,6 +106,26 @@ int attn_sink_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v,
                   attn_bf16* out, float* lse, void* stream);
 
 /*
+ * attn_sink_fwd with explicit row strides, for packed layouts (the varlen
+ * forward functions of flash-attention PR "feat: Implement Sink Attention",
+ * Key Changes, come in packed-QKV and packed-KV forms).  q_row_stride,
+ * k_row_stride, v_row_stride are the distances in elements between
+ * consecutive token rows of q, k and v (0: contiguous, heads * head_dim).
+ * Within a row the heads stay contiguous, head_dim elements apart.  A packed
+ * (total, hq + 2*hkv, head_dim) QKV buffer is q = base, k = base + hq*head_dim,
+ * v = base + (hq+hkv)*head_dim, all with row stride (hq + 2*hkv)*head_dim.
+ * Strides must be 0 or >= heads*head_dim and multiples of 8; out stays
+ * contiguous.  Everything else as in attn_sink_fwd.
+ */
+int attn_sink_fwd_strided(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v,
+                          long long q_row_stride, long long k_row_stride, long long v_row_stride,
+                          const float* sink, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                          int batch, int total_q, int total_k, int hq, int hkv, int head_dim,
+                          int max_seqlen_q, int max_seqlen_k,
+                          int win_first, int win_last, int causal, float scale,
+                          attn_bf16* out, float* lse, void* stream);
+
+/*
  * Paged single-token decode with a sink and optional first/last-window
  * selection.  Pages: sglang PR "openai oss attention sink support with trtllm-gen backend" (Highlights: the decode path passes
  * sink=); sglang PR "To implement attention-sink" (page table rows built from the first and last
@@ -260,6 +280,24 @@ int attn_sink_bwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, co
                   int max_seqlen_q, int max_seqlen_k,
                   int win_first, int win_last, int causal, float scale,
                   attn_bf16* dq, attn_bf16* dk, attn_bf16* dv, float* dsink, void* stream);
+
+/*
+ * attn_sink_bwd with explicit row strides for q, k, v (inputs) and dq, dk, dv
+ * (outputs), for packed QKV / KV layouts (as in attn_sink_fwd_strided; a packed
+ * dQKV output uses the same offsets and stride as the packed QKV input).  out,
+ * lse and dout stay contiguous.  With any of the dk / dv strides non-zero, dk/dv
+ * rows past cu_seqlens_k[batch] are left untouched (instead of zeroed).
+ */
+int attn_sink_bwd_strided(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v,
+                          long long q_row_stride, long long k_row_stride, long long v_row_stride,
+                          const float* sink, const attn_bf16* out, const float* lse,
+                          const attn_bf16* dout, const int32_t* cu_seqlens_q,
+                          const int32_t* cu_seqlens_k, int batch, int total_q, int total_k, int hq,
+                          int hkv, int head_dim, int max_seqlen_q, int max_seqlen_k,
+                          int win_first, int win_last, int causal, float scale,
+                          attn_bf16* dq, attn_bf16* dk, attn_bf16* dv,
+                          long long dq_row_stride, long long dk_row_stride, long long dv_row_stride,
+                          float* dsink, void* stream);
 
 /*
  * The visible token ranges of each decode request, as the decode kernels

@@ -8,11 +8,14 @@ from ._lib import (  # noqa: F401
     EXPORTS,
     AttnSinkError,
     attn_sink_bwd,
+    attn_sink_bwd_qkvpacked,
     attn_sink_decode_paged,
     attn_sink_decode_paged_append,
     attn_sink_decode_paged_noalloc,
     attn_sink_fwd,
+    attn_sink_fwd_kvpacked,
     attn_sink_fwd_paged,
+    attn_sink_fwd_qkvpacked,
     attn_sink_kv_append,
     attn_sink_visible_ranges,
     attn_sink_visible_slots,

@@ -21,6 +21,7 @@ DEV_PAGE_OOB, DEV_SEQLEN_OOB, DEV_TIMEOUT = 1, 2, 4
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
+_L = ctypes.c_longlong
 _F = ctypes.c_float
 
 _SIGS = {
@@ -31,6 +32,10 @@ _SIGS = {
                                        _P, _P],
     "attn_sink_bwd": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I,
                       _I, _F, _P, _P, _P, _P, _P],
+    "attn_sink_fwd_strided": [_P, _P, _P, _L, _L, _L, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I,
+                              _I, _F, _P, _P, _P],
+    "attn_sink_bwd_strided": [_P, _P, _P, _L, _L, _L, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                              _I, _I, _I, _I, _F, _P, _P, _P, _L, _L, _L, _P, _P],
     "attn_sink_kv_append": [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P],
     "attn_sink_decode_paged_append": [_P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _I, _I, _F,
                                       _P, _P, _P],
@@ -155,6 +160,94 @@ def attn_sink_decode_paged_noalloc(q, k_cache, v_cache, page_table, seqlens, sin
     return attn_sink_decode_paged(q, k_cache, v_cache, page_table, seqlens, sink, win_first, win_last,
                                   scale, out, lse, return_lse, stream,
                                   _entry="attn_sink_decode_paged_noalloc")
+
+
+def _row_view(base, col0, heads, d):
+    """(pointer, row stride) of columns [col0, col0 + heads) of a (T, C, d) buffer."""
+    if base.dim() != 3 or base.stride(2) != 1 or base.stride(1) != d:
+        raise TypeError("packed buffer must be (T, C, d) with contiguous rows")
+    return ctypes.c_void_p(base.data_ptr() + col0 * d * base.element_size()), base.stride(0)
+
+
+def attn_sink_fwd_qkvpacked(qkv, hkv, sink, cu_seqlens_q, max_seqlen_q, win_first=0, win_last=0,
+                            causal=True, scale=0.0, out=None, lse=None, return_lse=True, stream=None):
+    """Self-attention forward on a packed (T, hq + 2*hkv, d) QKV buffer (a
+    (T, 3, H, d) buffer is the same with hkv = H after a view).  Returns (out, lse)."""
+    if qkv.dim() == 4:
+        qkv = qkv.reshape(qkv.shape[0], -1, qkv.shape[-1])
+    _need(qkv, torch.bfloat16, "qkv")
+    _need(sink, torch.float32, "sink")
+    _need(cu_seqlens_q, torch.int32, "cu_seqlens_q")
+    T, C, d = qkv.shape
+    hq = C - 2 * hkv
+    qp, rs = _row_view(qkv, 0, hq, d)
+    kp, _ = _row_view(qkv, hq, hkv, d)
+    vp, _ = _row_view(qkv, hq + hkv, hkv, d)
+    if out is None:
+        out = torch.empty((T, hq, d), dtype=qkv.dtype, device=qkv.device)
+    if lse is None and return_lse:
+        lse = torch.empty((hq, T), dtype=torch.float32, device=qkv.device)
+    rc = lib().attn_sink_fwd_strided(qp, kp, vp, rs, rs, rs, _ptr(sink), _ptr(cu_seqlens_q), _ptr(cu_seqlens_q),
+                                     cu_seqlens_q.numel() - 1, T, T, hq, hkv, d, int(max_seqlen_q),
+                                     int(max_seqlen_q), int(win_first), int(win_last), 1 if causal else 0,
+                                     float(scale), _ptr(out), _ptr(lse), _stream(stream))
+    _check("attn_sink_fwd_strided", rc)
+    return out, lse
+
+
+def attn_sink_fwd_kvpacked(q, kv, sink, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, win_first=0,
+                           win_last=0, causal=True, scale=0.0, out=None, lse=None, return_lse=True,
+                           stream=None):
+    """Forward with a packed (Tk, 2, hkv, d) KV buffer.  Returns (out, lse)."""
+    _need(q, torch.bfloat16, "q")
+    _need(kv, torch.bfloat16, "kv")
+    _need(sink, torch.float32, "sink")
+    tq, hq, d = q.shape
+    tk, _, hkv, _ = kv.shape
+    kv3 = kv.reshape(tk, 2 * hkv, d)
+    kp, rs = _row_view(kv3, 0, hkv, d)
+    vp, _ = _row_view(kv3, hkv, hkv, d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((hq, tq), dtype=torch.float32, device=q.device)
+    rc = lib().attn_sink_fwd_strided(_ptr(q), kp, vp, 0, rs, rs, _ptr(sink), _ptr(cu_seqlens_q),
+                                     _ptr(cu_seqlens_k), cu_seqlens_q.numel() - 1, tq, tk, hq, hkv, d,
+                                     int(max_seqlen_q), int(max_seqlen_k), int(win_first), int(win_last),
+                                     1 if causal else 0, float(scale), _ptr(out), _ptr(lse), _stream(stream))
+    _check("attn_sink_fwd_strided", rc)
+    return out, lse
+
+
+def attn_sink_bwd_qkvpacked(qkv, hkv, sink, out, lse, dout, cu_seqlens_q, max_seqlen_q, win_first=0,
+                            win_last=0, causal=True, scale=0.0, dqkv=None, dsink=None, stream=None):
+    """Backward of attn_sink_fwd_qkvpacked; returns (dqkv, dsink or None), dqkv in
+    the layout of qkv."""
+    shape4 = qkv.shape if qkv.dim() == 4 else None
+    if qkv.dim() == 4:
+        qkv = qkv.reshape(qkv.shape[0], -1, qkv.shape[-1])
+    for t, n in ((qkv, "qkv"), (out, "out"), (dout, "dout")):
+        _need(t, torch.bfloat16, n)
+    _need(sink, torch.float32, "sink")
+    _need(lse, torch.float32, "lse")
+    T, C, d = qkv.shape
+    hq = C - 2 * hkv
+    dqkv = torch.empty_like(qkv) if dqkv is None else dqkv.reshape(T, C, d)
+    if sink is not None and dsink is None:
+        dsink = torch.empty_like(sink)
+    qp, rs = _row_view(qkv, 0, hq, d)
+    kp, _ = _row_view(qkv, hq, hkv, d)
+    vp, _ = _row_view(qkv, hq + hkv, hkv, d)
+    dqp, drs = _row_view(dqkv, 0, hq, d)
+    dkp, _ = _row_view(dqkv, hq, hkv, d)
+    dvp, _ = _row_view(dqkv, hq + hkv, hkv, d)
+    rc = lib().attn_sink_bwd_strided(qp, kp, vp, rs, rs, rs, _ptr(sink), _ptr(out), _ptr(lse), _ptr(dout),
+                                     _ptr(cu_seqlens_q), _ptr(cu_seqlens_q), cu_seqlens_q.numel() - 1, T, T, hq,
+                                     hkv, d, int(max_seqlen_q), int(max_seqlen_q), int(win_first),
+                                     int(win_last), 1 if causal else 0, float(scale), dqp, dkp, dvp, drs, drs,
+                                     drs, _ptr(dsink), _stream(stream))
+    _check("attn_sink_bwd_strided", rc)
+    return (dqkv.reshape(shape4) if shape4 is not None else dqkv), dsink
 
 
 def attn_sink_kv_append(k_new, v_new, k_cache, v_cache, page_table, seqlens, cu_new=None,

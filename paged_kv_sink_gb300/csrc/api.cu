@@ -288,12 +288,24 @@ static int validate_varlen(const char* who, const void* q, const void* k, const 
     return ATTN_SINK_OK;
 }
 
-int attn_sink_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, const float* sink,
-                  const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch, int total_q,
-                  int total_k, int hq, int hkv, int head_dim, int max_seqlen_q, int max_seqlen_k,
-                  int win_first, int win_last, int causal, float scale, attn_bf16* out, float* lse,
-                  void* stream) {
-    t_last_error.clear();
+}  // extern "C"
+
+namespace {
+
+// A row stride (elements) is 0 (contiguous) or covers the row's heads and keeps
+// every row 16-byte aligned.
+int check_stride(const char* who, const char* name, long long rs, int heads) {
+    if (rs == 0) return ATTN_SINK_OK;
+    if (rs < (long long)heads * 64 || rs % 8)
+        return fail(ATTN_SINK_ERR_INVALID, "%s: %s row stride %lld must be 0 or >= heads*64 and a multiple of 8", who,
+                    name, rs);
+    return ATTN_SINK_OK;
+}
+
+int fwd_impl(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, long long q_rs, long long k_rs,
+             long long v_rs, const float* sink, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch,
+             int total_q, int total_k, int hq, int hkv, int head_dim, int max_seqlen_q, int max_seqlen_k,
+             int win_first, int win_last, int causal, float scale, attn_bf16* out, float* lse, void* stream) {
     int rc = validate_varlen("fwd", q, k, v, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, hq, hkv, head_dim,
                              max_seqlen_q, max_seqlen_k, win_first, win_last, causal);
     if (rc != ATTN_SINK_OK || batch == 0 || max_seqlen_q == 0 || total_q == 0) return rc;
@@ -320,10 +332,44 @@ int attn_sink_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, co
     a.win_last = win_last;
     a.causal = causal ? 1 : 0;
     a.scale = resolve_scale(scale, head_dim);
+    a.q_rs = q_rs;
+    a.k_rs = k_rs;
+    a.v_rs = v_rs;
     std::string err;
     cudaError_t e = attn::prefill::launch_fwd(a, static_cast<cudaStream_t>(stream), &err);
     if (e != cudaSuccess) return fail(ATTN_SINK_ERR_CUDA, "fwd: %s: %s", err.c_str(), cudaGetErrorString(e));
     return ATTN_SINK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_sink_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, const float* sink,
+                  const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch, int total_q,
+                  int total_k, int hq, int hkv, int head_dim, int max_seqlen_q, int max_seqlen_k,
+                  int win_first, int win_last, int causal, float scale, attn_bf16* out, float* lse,
+                  void* stream) {
+    t_last_error.clear();
+    return fwd_impl(q, k, v, 0, 0, 0, sink, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, hq, hkv, head_dim,
+                    max_seqlen_q, max_seqlen_k, win_first, win_last, causal, scale, out, lse, stream);
+}
+
+int attn_sink_fwd_strided(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, long long q_row_stride,
+                          long long k_row_stride, long long v_row_stride, const float* sink,
+                          const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch, int total_q,
+                          int total_k, int hq, int hkv, int head_dim, int max_seqlen_q, int max_seqlen_k,
+                          int win_first, int win_last, int causal, float scale, attn_bf16* out, float* lse,
+                          void* stream) {
+    t_last_error.clear();
+    int rc;
+    if ((rc = check_stride("fwd_strided", "q", q_row_stride, hq)) != ATTN_SINK_OK ||
+        (rc = check_stride("fwd_strided", "k", k_row_stride, hkv)) != ATTN_SINK_OK ||
+        (rc = check_stride("fwd_strided", "v", v_row_stride, hkv)) != ATTN_SINK_OK)
+        return rc;
+    return fwd_impl(q, k, v, q_row_stride, k_row_stride, v_row_stride, sink, cu_seqlens_q, cu_seqlens_k, batch,
+                    total_q, total_k, hq, hkv, head_dim, max_seqlen_q, max_seqlen_k, win_first, win_last, causal,
+                    scale, out, lse, stream);
 }
 
 int attn_sink_fwd_paged(const attn_bf16* q, const attn_bf16* k_new, const attn_bf16* v_new, attn_bf16* k_cache,
@@ -392,13 +438,15 @@ int attn_sink_fwd_paged(const attn_bf16* q, const attn_bf16* k_new, const attn_b
     return ATTN_SINK_OK;
 }
 
-int attn_sink_bwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, const float* sink,
-                  const attn_bf16* out, const float* lse, const attn_bf16* dout,
-                  const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch, int total_q,
-                  int total_k, int hq, int hkv, int head_dim, int max_seqlen_q, int max_seqlen_k,
-                  int win_first, int win_last, int causal, float scale, attn_bf16* dq, attn_bf16* dk,
-                  attn_bf16* dv, float* dsink, void* stream) {
-    t_last_error.clear();
+}  // extern "C"
+
+namespace {
+
+int bwd_impl(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, const long long* rs, const float* sink,
+             const attn_bf16* out, const float* lse, const attn_bf16* dout, const int32_t* cu_seqlens_q,
+             const int32_t* cu_seqlens_k, int batch, int total_q, int total_k, int hq, int hkv, int head_dim,
+             int max_seqlen_q, int max_seqlen_k, int win_first, int win_last, int causal, float scale,
+             attn_bf16* dq, attn_bf16* dk, attn_bf16* dv, float* dsink, void* stream) {
     int rc = validate_varlen("bwd", q, k, v, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, hq, hkv, head_dim,
                              max_seqlen_q, max_seqlen_k, win_first, win_last, causal);
     if (rc != ATTN_SINK_OK) return rc;
@@ -436,6 +484,12 @@ int attn_sink_bwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, co
     a.win_last = win_last;
     a.causal = causal ? 1 : 0;
     a.scale = resolve_scale(scale, head_dim);
+    a.q_rs = rs[0];
+    a.k_rs = rs[1];
+    a.v_rs = rs[2];
+    a.dq_rs = rs[3];
+    a.dk_rs = rs[4];
+    a.dv_rs = rs[5];
     size_t ws_bytes = attn::bwd::workspace_bytes(a);
     Scratch ws;
     cudaError_t e = ws.alloc(ws_bytes, s);
@@ -444,6 +498,43 @@ int attn_sink_bwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, co
     e = attn::bwd::launch(a, ws.ptr, ws_bytes, s, &err);
     if (e != cudaSuccess) return fail(ATTN_SINK_ERR_CUDA, "bwd: %s: %s", err.c_str(), cudaGetErrorString(e));
     return ATTN_SINK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_sink_bwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, const float* sink,
+                  const attn_bf16* out, const float* lse, const attn_bf16* dout,
+                  const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch, int total_q,
+                  int total_k, int hq, int hkv, int head_dim, int max_seqlen_q, int max_seqlen_k,
+                  int win_first, int win_last, int causal, float scale, attn_bf16* dq, attn_bf16* dk,
+                  attn_bf16* dv, float* dsink, void* stream) {
+    t_last_error.clear();
+    const long long rs[6] = {0, 0, 0, 0, 0, 0};
+    return bwd_impl(q, k, v, rs, sink, out, lse, dout, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, hq,
+                    hkv, head_dim, max_seqlen_q, max_seqlen_k, win_first, win_last, causal, scale, dq, dk, dv,
+                    dsink, stream);
+}
+
+int attn_sink_bwd_strided(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, long long q_row_stride,
+                          long long k_row_stride, long long v_row_stride, const float* sink,
+                          const attn_bf16* out, const float* lse, const attn_bf16* dout,
+                          const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch, int total_q,
+                          int total_k, int hq, int hkv, int head_dim, int max_seqlen_q, int max_seqlen_k,
+                          int win_first, int win_last, int causal, float scale, attn_bf16* dq, attn_bf16* dk,
+                          attn_bf16* dv, long long dq_row_stride, long long dk_row_stride,
+                          long long dv_row_stride, float* dsink, void* stream) {
+    t_last_error.clear();
+    int rc;
+    const long long rs[6] = {q_row_stride, k_row_stride, v_row_stride, dq_row_stride, dk_row_stride,
+                             dv_row_stride};
+    const char* names[6] = {"q", "k", "v", "dq", "dk", "dv"};
+    for (int i = 0; i < 6; ++i)
+        if ((rc = check_stride("bwd_strided", names[i], rs[i], (i % 3) == 0 ? hq : hkv)) != ATTN_SINK_OK) return rc;
+    return bwd_impl(q, k, v, rs, sink, out, lse, dout, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, hq,
+                    hkv, head_dim, max_seqlen_q, max_seqlen_k, win_first, win_last, causal, scale, dq, dk, dv,
+                    dsink, stream);
 }
 
 int attn_sink_device_status(void* stream) {

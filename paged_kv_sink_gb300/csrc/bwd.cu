@@ -73,8 +73,9 @@ struct MainParams {
     const float* lse;      // (hq, total_q)
     const float* dvec;     // (hq, total_q)
     float* dq_accum;       // (total_q, hq, D) fp32
-    __nv_bfloat16* dk;     // (total_k, hkv, D)
-    __nv_bfloat16* dv;
+    __nv_bfloat16* dk;     // (total_k, hkv, D), rows dk_rs elements apart
+    __nv_bfloat16* dv;     // rows dv_rs elements apart
+    long long dk_rs, dv_rs;
     int hq, hkv, group, total_q, total_k;
     int win_first, win_last, causal;
     float scale, scale_log2;
@@ -459,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool have = ok && T > 0;
         if (have) tc_fence_after();
         const int kpos = j0 + i;
-        const size_t rowoff = ((size_t)(k_start + kpos) * p.hkv + kvh) * D;
+        const size_t rowoff = (size_t)(k_start + kpos) * (size_t)(ch == 0 ? p.dk_rs : p.dv_rs) + (size_t)kvh * D;
         const uint32_t col = ch == 0 ? cDK : cDV;
         const float f = 1.f;  // dK: the scale rides on dS
         __nv_bfloat16* outp = ch == 0 ? p.dk : p.dv;
@@ -552,17 +553,21 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
     }
 }
 
-__global__ void bwd_dq_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq, size_t n4) {
+// acc holds rows of row4 float4 (hq * 64 / 4); dq rows are dq_rs4 uint2 apart.
+__global__ void bwd_dq_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq, size_t n4,
+                                      int row4, long long dq_rs4) {
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
         const float4 v = acc[i];
-        dq[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+        const size_t row = i / (size_t)row4, c = i - row * (size_t)row4;
+        dq[row * (size_t)dq_rs4 + c] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
     }
 }
 
 // ---------------------------------------------------------------------------
 // Host side
 
-cudaError_t make_map(CUtensorMap* m, const void* base, int heads, long long rows, std::string* what);
+cudaError_t make_map(CUtensorMap* m, const void* base, int heads, long long rows, std::string* what,
+                     long long row_stride = 0);
 cudaError_t make_map_dq(CUtensorMap* m, const float* base, int heads, long long rows, std::string* what);
 
 size_t workspace_bytes(const Args& a) {
@@ -584,14 +589,15 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-cudaError_t make_map(CUtensorMap* m, const void* base, int heads, long long rows, std::string* what) {
+cudaError_t make_map(CUtensorMap* m, const void* base, int heads, long long rows, std::string* what,
+                     long long row_stride) {
     auto fn = encode_fn();
     if (!fn) {
         *what = "cuTensorMapEncodeTiled unavailable";
         return cudaErrorNotSupported;
     }
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1)};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)D * 2 * heads};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)(row_stride > 0 ? row_stride : (long long)D * heads) * 2};
     cuuint32_t box[3] = {(cuuint32_t)D, 1, 128};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
@@ -635,9 +641,11 @@ cudaError_t launch(const Args& a, void* workspace, size_t ws_bytes, cudaStream_t
         *what = "memset dsink";
         return e;
     }
-    // dK/dV rows of keys no CTA visits (past every request's end) are zero.
-    if ((e = cudaMemsetAsync(a.dk, 0, (size_t)a.total_k * a.hkv * D * 2, s)) != cudaSuccess ||
-        (e = cudaMemsetAsync(a.dv, 0, (size_t)a.total_k * a.hkv * D * 2, s)) != cudaSuccess) {
+    // dK/dV rows of keys no CTA visits (past every request's end) are zero
+    // (contiguous outputs only: a strided output shares its rows with other tensors).
+    const bool dkv_contig = a.dk_rs <= 0 && a.dv_rs <= 0;
+    if (dkv_contig && ((e = cudaMemsetAsync(a.dk, 0, (size_t)a.total_k * a.hkv * D * 2, s)) != cudaSuccess ||
+                       (e = cudaMemsetAsync(a.dv, 0, (size_t)a.total_k * a.hkv * D * 2, s)) != cudaSuccess)) {
         *what = "memset dk/dv";
         return e;
     }
@@ -657,9 +665,9 @@ cudaError_t launch(const Args& a, void* workspace, size_t ws_bytes, cudaStream_t
     }
     if (a.total_q > 0 && a.total_k > 0 && a.max_seqlen_k > 0) {
         CUtensorMap tq, tk, tv, tdo, tdq;
-        if ((e = make_map(&tq, a.q, a.hq, a.total_q, what)) != cudaSuccess) return e;
-        if ((e = make_map(&tk, a.k, a.hkv, a.total_k, what)) != cudaSuccess) return e;
-        if ((e = make_map(&tv, a.v, a.hkv, a.total_k, what)) != cudaSuccess) return e;
+        if ((e = make_map(&tq, a.q, a.hq, a.total_q, what, a.q_rs)) != cudaSuccess) return e;
+        if ((e = make_map(&tk, a.k, a.hkv, a.total_k, what, a.k_rs)) != cudaSuccess) return e;
+        if ((e = make_map(&tv, a.v, a.hkv, a.total_k, what, a.v_rs)) != cudaSuccess) return e;
         if ((e = make_map(&tdo, a.dout, a.hq, a.total_q, what)) != cudaSuccess) return e;
         if ((e = make_map_dq(&tdq, dq_accum, a.hq, a.total_q, what)) != cudaSuccess) return e;
         MainParams p;
@@ -670,6 +678,8 @@ cudaError_t launch(const Args& a, void* workspace, size_t ws_bytes, cudaStream_t
         p.dq_accum = dq_accum;
         p.dk = reinterpret_cast<__nv_bfloat16*>(a.dk);
         p.dv = reinterpret_cast<__nv_bfloat16*>(a.dv);
+        p.dk_rs = a.dk_rs > 0 ? a.dk_rs : (long long)a.hkv * D;
+        p.dv_rs = a.dv_rs > 0 ? a.dv_rs : (long long)a.hkv * D;
         p.hq = a.hq;
         p.hkv = a.hkv;
         p.group = a.hq / a.hkv;
@@ -697,8 +707,9 @@ cudaError_t launch(const Args& a, void* workspace, size_t ws_bytes, cudaStream_t
         const size_t n4 = (size_t)a.total_q * a.hq * D / 4;
         int blocks = (int)((n4 + 255) / 256);
         if (blocks > 152 * 16) blocks = 152 * 16;
+        const long long dq_rs = a.dq_rs > 0 ? a.dq_rs : (long long)a.hq * D;
         bwd_dq_convert_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(dq_accum),
-                                                    reinterpret_cast<uint2*>(a.dq), n4);
+                                                    reinterpret_cast<uint2*>(a.dq), n4, a.hq * D / 4, dq_rs / 4);
         if ((e = cudaGetLastError()) != cudaSuccess) {
             *what = "dq convert launch";
             return e;

@@ -27,6 +27,10 @@ struct Args {
     float* dsink;
     int batch, total_q, total_k, hq, hkv, head_dim, max_seqlen_q, max_seqlen_k, win_first, win_last, causal;
     float scale;
+    // Row strides in elements of q, k, v (inputs) and dq, dk, dv (outputs); 0 means
+    // contiguous rows (heads * 64).  With any output stride set, dk/dv rows past
+    // cu_seqlens_k[batch] are left untouched instead of zeroed.
+    long long q_rs = 0, k_rs = 0, v_rs = 0, dq_rs = 0, dk_rs = 0, dv_rs = 0;
 };
 
 size_t workspace_bytes(const Args& a);

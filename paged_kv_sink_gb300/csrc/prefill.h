@@ -27,6 +27,8 @@ struct FwdArgs {
     const int32_t* page_table = nullptr;
     const int32_t* seqlens_k = nullptr;
     int max_pages = 0, page_size = 0, num_pages = 0;
+    // Row strides of q, k, v in elements (0: contiguous rows of heads * 64).
+    long long q_rs = 0, k_rs = 0, v_rs = 0;
 };
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s, std::string* what);

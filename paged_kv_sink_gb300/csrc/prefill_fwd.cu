@@ -482,15 +482,16 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // (rows, heads, 64) bf16 tensor viewed as a 3-D map {d, head, row}; box {64, 1, box_rows}.
+// Rows are row_stride elements apart (0: heads * 64, i.e. contiguous).
 cudaError_t make_map(CUtensorMap* m, const void* base, int heads, long long rows, int box_rows,
-                     std::string* what) {
+                     std::string* what, long long row_stride = 0) {
     auto fn = encode_fn();
     if (!fn) {
         *what = "cuTensorMapEncodeTiled unavailable";
         return cudaErrorNotSupported;
     }
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1)};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)D * 2 * heads};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)(row_stride > 0 ? row_stride : (long long)D * heads) * 2};
     cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)box_rows};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
@@ -514,9 +515,9 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s, std::string* what) {
         seg_shift = page_shift < 7 ? page_shift : 7;  // segments of min(page_size, 128) rows
     }
     const long long krows = paged ? (long long)a.num_pages * a.page_size : a.total_k;
-    if ((e = make_map(&tq, a.q, a.hq, a.total_q, BM, what)) != cudaSuccess) return e;
-    if ((e = make_map(&tk, a.k, a.hkv, krows, 1 << seg_shift, what)) != cudaSuccess) return e;
-    if ((e = make_map(&tv, a.v, a.hkv, krows, 1 << seg_shift, what)) != cudaSuccess) return e;
+    if ((e = make_map(&tq, a.q, a.hq, a.total_q, BM, what, a.q_rs)) != cudaSuccess) return e;
+    if ((e = make_map(&tk, a.k, a.hkv, krows, 1 << seg_shift, what, a.k_rs)) != cudaSuccess) return e;
+    if ((e = make_map(&tv, a.v, a.hkv, krows, 1 << seg_shift, what, a.v_rs)) != cudaSuccess) return e;
     Params p;
     p.page_table = a.page_table;
     p.seqlens_k = a.seqlens_k;
