@@ -71,7 +71,9 @@ enum {
 enum {
     ATTN_SINK_DEV_PAGE_OOB = 1,      /* a page-table entry was outside [0, num_pages)       */
     ATTN_SINK_DEV_SEQLEN_OOB = 2,    /* a sequence length exceeded max_pages * page_size    */
-    ATTN_SINK_DEV_TIMEOUT = 4        /* a pipeline wait ran out of time; the kernel gave up */
+    ATTN_SINK_DEV_TIMEOUT = 4,       /* a pipeline wait ran out of time; the kernel gave up */
+    ATTN_SINK_DEV_LAYOUT = 8         /* the dynamic shared-memory base was not 1024-byte
+                                        aligned; the forward kernel did nothing            */
 };
 
 /*

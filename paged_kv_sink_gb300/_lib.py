@@ -17,7 +17,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libattn_sink.so")
 
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE = 0, -1, -2, -3, -4
-DEV_PAGE_OOB, DEV_SEQLEN_OOB, DEV_TIMEOUT = 1, 2, 4
+DEV_PAGE_OOB, DEV_SEQLEN_OOB, DEV_TIMEOUT, DEV_LAYOUT = 1, 2, 4, 8
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int

@@ -12,11 +12,12 @@
 // One CTA = 128 query rows of one query head; two CTAs share an SM, so the
 // tensor core interleaves two independent pipelines.
 //   warp 0      TMA producer: Q once, then the K tiles (3-stage ring)
-//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer:
+//   warp 1      TMEM allocator and tcgen05.mma issuer (converged warp, elect.sync):
 //               S = Q K^T (128x128 fp32, A and B from shared memory),
 //               O += P V  (128x64 fp32, A = P from TMEM, B = V from shared memory)
-//   warp 2      TMA producer of the V tiles (2-stage ring: a V stage is needed
-//               only when the P V product is issued)
+//   warp 2      TMA producer of the V tiles (3-stage ring)
+// With a paged cache the producers fetch each tile as page segments through
+// the page table (one TMA copy per segment).
 //   warp 3      idle (completes warpgroup 0 for the register split)
 //   warps 4..7  softmax warpgroup; thread = query row.
 // TMEM (256 columns): S at 0, O at 128, P (bf16 pairs) at 192.
@@ -41,7 +42,7 @@ constexpr int BM = 128;
 constexpr int BN = 128;
 constexpr int D = 64;
 constexpr int KSTAGE = 3;
-constexpr int VSTAGE = 2;
+constexpr int VSTAGE = 3;
 constexpr int kThreads = 256;
 // Two CTAs per SM: 128 registers per thread at launch.  setmaxnreg moves them
 // from warpgroup 0 (TMA + MMA) to the softmax warpgroup:
@@ -98,7 +99,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const Params p) {
     extern __shared__ uint8_t smem_raw[];
-    Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // Two CTAs per SM only fit without alignment slack: the dynamic shared base
+    // (after the 1 KB the hardware reserves per CTA) must already be 1024-aligned
+    // for the 128-byte swizzle atoms.  Checked, never assumed.
+    Smem& S = *reinterpret_cast<Smem*>(smem_raw);
+    if (smem_u32(smem_raw) & 1023u) {
+        if (threadIdx.x == 0) raise_status(ATTN_SINK_DEV_LAYOUT);
+        return;
+    }
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Grid (head, row tile, request): the CTAs in flight share one request's K/V
@@ -539,7 +547,7 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s, std::string* what) {
     p.win_last = a.win_last;
     p.causal = a.causal;
     p.scale_log2 = a.scale * ATTN_LOG2E;
-    const size_t smem = sizeof(Smem) + 1024;
+    const size_t smem = sizeof(Smem);
     e = cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) {
         *what = "smem attribute";
