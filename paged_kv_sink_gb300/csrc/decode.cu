@@ -420,9 +420,19 @@ Plan make_plan(const Args& a) {
     }
     if (nvis_max < 1) nvis_max = 1;
     const long long units = (long long)a.batch * a.hkv * pl.hblocks;
-    const long long want = 8LL * num_sms_cached();
-    int split = 512;
-    while (split > 64 && units * ((nvis_max / 2 + split - 1) / split) < want) split /= 2;
+    // Split size: aim at about two waves of resident CTAs (the shared-memory
+    // ring allows 4 CTAs per SM at d 64, 2 at d 128), then clamp so that a
+    // split streams at least 256 tokens (the ring's fill and drain amortised)
+    // and at most 256 KB of K per split (2048 tokens at d 64, 1024 at d 128):
+    // longer splits leave too few CTAs, shorter ones are latency-bound waves.
+    const long long slots = (long long)num_sms_cached() * (a.head_dim == 64 ? 4 : 2);
+    const long long per_unit = (2 * slots + units - 1) / units;  // splits wanted per (request, head block)
+    long long sp = (nvis_max + per_unit - 1) / per_unit;
+    sp = (sp + kChunk - 1) / kChunk * kChunk;
+    const long long sp_max = 2048LL * 64 / a.head_dim;
+    if (sp > sp_max) sp = sp_max;
+    if (sp < 256) sp = 256;
+    const int split = (int)sp;
     pl.split_tokens = split;
     pl.max_splits = (int)((nvis_max + split - 1) / split);
     pl.part_o_bytes = (size_t)a.batch * a.hq * pl.max_splits * a.head_dim * sizeof(float);

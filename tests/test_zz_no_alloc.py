@@ -37,6 +37,10 @@ def test_noalloc_matches_allocating_entry_point_twice(ext, case):
     else:  # partials of the default split exceed the static array: fewer, longer splits
         dc = wl.make_decode(seqlens=[20000] * 64, hq=64, hkv=8, d=64, page_size=16,
                             sink=("uniform", -2.0, 4.0), seed=22)
+        # the plan sizes splits for the page table's capacity (4096 pages = 65536
+        # tokens): 32 splits of 2048 tokens, 34.6 MB of partials > 32 MiB
+        pad = torch.full((64, 4096 - dc.page_table.shape[1]), -1, dtype=torch.int32)
+        dc.page_table = torch.cat([dc.page_table, pad], dim=1).contiguous()
     (q, kc, vc, pt, sl), sink = _dev(dc)
     ref_o, ref_l = ext.attn_sink_decode_paged(q, kc, vc, pt, sl, sink, dc.win_first, dc.win_last)
     torch.cuda.synchronize()
