@@ -39,14 +39,14 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel source it was measured on and is reported only while that source is
 # unchanged.
 NCU_TRAFFIC = {
-    # profiles/fwd_kernel_extend_varlen.md: 444.4 MB read + 259.2 MB written per launch
-    "fwd_kernel/extend_varlen": {"src": "d72806b19cb54231", "bytes": 703_589_376},
-    # profiles/bwd_main_kernel_train.md: 2.549 GB read + 1.126 GB written per launch
-    "bwd_main_kernel/train": {"src": "e7c5b15167ee58ec", "bytes": 3_675_104_000},
-    # profiles/decode_split_kernel_decode_sink.md: decode_split_kernel, 1.943 GB + 0.033 GB
-    "decode/decode_sink": {"src": "02720d9c34caae7c", "bytes": 1_976_352_288},
-    # profiles/decode_split_kernel_decode_window.md: decode_split_kernel, 1.074 GB + 0.011 GB
-    "decode/decode_window": {"src": "02720d9c34caae7c", "bytes": 1_084_827_960},
+    # profiles/fwd_kernel_extend_varlen.md: 443.2 MB read + 259.3 MB written per launch
+    "fwd_kernel/extend_varlen": {"src": "5da617d4d921001f", "bytes": 702_455_552},
+    # profiles/bwd_main_kernel_train.md: 2.432 GB read + 1.093 GB written per launch
+    "bwd_main_kernel/train": {"src": "fdd13635abf852bb", "bytes": 3_525_792_000},
+    # profiles/decode_split_kernel_decode_sink.md: decode_split_kernel, 1.944 GB + 0.011 GB
+    "decode/decode_sink": {"src": "74c2b03b3cdc9cb0", "bytes": 1_954_192_080},
+    # profiles/decode_split_kernel_decode_window.md: decode_split_kernel, 1.074 GB + 0.007 GB
+    "decode/decode_window": {"src": "74c2b03b3cdc9cb0", "bytes": 1_080_889_760},
 }
 
 
