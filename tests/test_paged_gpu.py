@@ -215,3 +215,73 @@ def test_extend_paged_full_size_sampled(ext):
     idx = np.concatenate([np.asarray(r) + cq[b] for b, r in rows.items()])
     assert_out_close(out.cpu()[idx], O[idx])
     assert_lse_close(lse.cpu()[:, idx], LSE[:, idx])
+
+
+def test_kv_append_bad_rows_are_skipped_and_flagged(ext):
+    """A page id outside the cache and a request with more new rows than cached
+    tokens are skipped (no write anywhere) and raise the device status bits."""
+    pe = wl.make_paged_extend(seqlens_q=[2, 3, 1], seqlens_k=[10, 2, 40], hq=2, hkv=2, d=64, page_size=16,
+                              seed=9, extra_pages=2)
+    pt = pe.page_table.clone()
+    pt[2, 2] = pe.k_cache.shape[0] + 7  # request 2's new token (position 39) lands in page index 2
+    dev = "cuda"
+    kc, vc = pe.k_cache.to(dev), pe.v_cache.to(dev)
+    ext.device_status()  # clear
+    ext.attn_sink_kv_append(pe.k_new.to(dev), pe.v_new.to(dev), kc, vc, pt.to(dev), pe.seqlens_k.to(dev),
+                            cu_new=pe.cu_seqlens_q.to(dev))
+    torch.cuda.synchronize()
+    bits = ext.device_status()
+    assert bits & ext._lib.DEV_PAGE_OOB and bits & ext._lib.DEV_SEQLEN_OOB
+    # request 0 is appended normally; request 1 (3 rows, 2 tokens): rows with t >= 0 are written,
+    # the one at t = -1 is skipped; request 2's row is skipped
+    want_k, _ = orc.kv_append(pe.k_cache, pe.v_cache, pe.page_table[:1], pe.seqlens_k[:1], pe.k_new[:2],
+                              pe.v_new[:2], 16, cu_new=torch.tensor([0, 2], dtype=torch.int32))
+    got = kc.cpu()
+    flat_got, flat_want, flat_old = got.reshape(-1, 2, 64), want_k.reshape(-1, 2, 64), pe.k_cache.reshape(-1, 2, 64)
+    pt0 = pe.page_table.numpy()
+    for t in (8, 9):  # request 0's two new rows
+        sl = orc.paged_slot(pt0, 0, t, 16)
+        assert torch.equal(flat_got[sl], flat_want[sl])
+    for t, r in ((0, 3), (1, 4)):  # request 1: rows 1 and 2 of its three land on tokens 0 and 1
+        sl = orc.paged_slot(pt0, 1, t, 16)
+        assert torch.equal(flat_got[sl], pe.k_new[r])
+    touched = {orc.paged_slot(pt0, 0, t, 16) for t in (8, 9)} | {orc.paged_slot(pt0, 1, t, 16) for t in (0, 1)}
+    for sl in range(flat_old.shape[0]):
+        if sl not in touched:
+            assert torch.equal(flat_got[sl], flat_old[sl])
+
+
+def test_fwd_paged_bad_page_is_flagged(ext):
+    pe = wl.make_paged_extend(seqlens_q=[64], seqlens_k=[200], hq=2, hkv=1, d=64, page_size=16, seed=2)
+    pt = pe.page_table.clone()
+    pt[0, 3] = -5
+    dev = "cuda"
+    ext.device_status()
+    ext.attn_sink_fwd_paged(pe.q.to(dev), pe.k_cache.to(dev), pe.v_cache.to(dev), pt.to(dev),
+                            pe.cu_seqlens_q.to(dev), pe.seqlens_k.to(dev), 64, 200, pe.sink.to(dev))
+    torch.cuda.synchronize()
+    assert ext.device_status() & ext._lib.DEV_PAGE_OOB
+
+
+def test_fwd_paged_empty_and_zero_length_requests(ext):
+    dev = "cuda"
+    # a request with no new rows and one with a single token between two regular ones
+    pe = wl.make_paged_extend(seqlens_q=[50, 0, 1, 70], seqlens_k=[90, 33, 1, 70], hq=4, hkv=2, d=64,
+                              page_size=32, seed=6)
+    out, lse = ext.attn_sink_fwd_paged(pe.q.to(dev), pe.k_cache.to(dev), pe.v_cache.to(dev),
+                                       pe.page_table.to(dev), pe.cu_seqlens_q.to(dev), pe.seqlens_k.to(dev),
+                                       pe.max_seqlen_q, pe.max_seqlen_k, pe.sink.to(dev), pe.k_new.to(dev),
+                                       pe.v_new.to(dev))
+    torch.cuda.synchronize()
+    assert ext.device_status() == 0
+    kw, vw = orc.kv_append(pe.k_cache, pe.v_cache, pe.page_table, pe.seqlens_k, pe.k_new, pe.v_new, 32,
+                           cu_new=pe.cu_seqlens_q)
+    O, LSE = orc.attn_fwd_paged(pe.q, kw, vw, pe.page_table, pe.seqlens_k, pe.cu_seqlens_q, 32, pe.sink)
+    assert_out_close(out.cpu(), O)
+    assert_lse_close(lse.cpu(), LSE)
+    # an empty batch is a no-op
+    q0 = torch.empty((0, 4, 64), dtype=torch.bfloat16, device=dev)
+    out0, _ = ext.attn_sink_fwd_paged(q0, pe.k_cache.to(dev), pe.v_cache.to(dev), pe.page_table[:0].to(dev),
+                                      torch.zeros(1, dtype=torch.int32, device=dev),
+                                      torch.zeros(0, dtype=torch.int32, device=dev), 0, 0, pe.sink.to(dev))
+    assert out0.shape == (0, 4, 64)
