@@ -175,11 +175,36 @@ def _flush_buf(torch, dev):
     return torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
 
 
-def time_steps(torch, fn, steps, warmup, flush):
+def max_over_ranks(torch, dist, values, device="cpu"):
+    """Element-wise maximum of per-rank values over all ranks (identity at N = 1)."""
+    if dist is None:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_rate(work_per_rank, world, seconds_max):
+    """Whole-job throughput: the work all ranks did over the slowest rank's time."""
+    return work_per_rank * world / seconds_max
+
+
+def rank_sync(torch, dist):
+    """Barrier across ranks (when there are several) and a device synchronise."""
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+def time_steps(torch, fn, steps, warmup, flush, sync=None):
+    """Per-step device times (CUDA events on the launching stream), L2 flushed
+    between steps outside the events; `sync` brackets the timed steps."""
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
+    if sync is not None:
+        sync()
     times = []
     for _ in range(steps):
         flush.zero_()
@@ -190,10 +215,12 @@ def time_steps(torch, fn, steps, warmup, flush):
         e1.record(stream)
         torch.cuda.synchronize()
         times.append(e0.elapsed_time(e1))
+    if sync is not None:
+        sync()
     return times
 
 
-def bench_extend(torch, ext, dev, p, steps, warmup, flush, peaks, peak_src):
+def bench_extend(torch, ext, dev, p, steps, warmup, flush, peaks, peak_src, sync=None):
     q, k, v = p.q.to(dev), p.k.to(dev), p.v.to(dev)
     sink = p.sink.to(dev)
     cq, ck = p.cu_seqlens_q.to(dev), p.cu_seqlens_k.to(dev)
@@ -203,7 +230,7 @@ def bench_extend(torch, ext, dev, p, steps, warmup, flush, peaks, peak_src):
     def step():
         ext.attn_sink_fwd(q, k, v, sink, cq, ck, p.max_seqlen_q, p.max_seqlen_k, out=out, lse=lse)
 
-    times = time_steps(torch, step, steps, warmup, flush)
+    times = time_steps(torch, step, steps, warmup, flush, sync)
     flops = fwd_flops(p)
     ms = sum(times) / len(times)
     achieved = flops / (ms * 1e-3) / 1e12
@@ -516,17 +543,13 @@ def main():
     p = wl.workload(args.workload, seed=rank)
     with ClockSampler(local) as clk:
         ms, flops, roof, times = bench_extend(torch, ext, dev, p, args.steps, args.warmup, flush, peaks,
-                                              peak_src)
+                                              peak_src, sync=lambda: rank_sync(torch, dist))
     clocks = clk.summary()
     e2e_ms, h2d, d2h = e2e_extend(torch, ext, dev, p, max(3, args.steps // 4), 2)
 
-    ms_max = ms
-    if dist is not None:
-        t = torch.tensor([ms, e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max, e2e_ms = float(t[0]), float(t[1])
-    value = flops * world / (ms_max * 1e-3) / 1e12
-    e2e_value = flops * world / (e2e_ms * 1e-3) / 1e12
+    ms_max, e2e_ms = max_over_ranks(torch, dist, [ms, e2e_ms], device=dev)
+    value = job_rate(flops, world, ms_max * 1e-3) / 1e12
+    e2e_value = job_rate(flops, world, e2e_ms * 1e-3) / 1e12
 
     extra = {}
     if not args.no_extra:
