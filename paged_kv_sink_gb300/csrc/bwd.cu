@@ -194,45 +194,69 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp < 4) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtrl));
-        if (warp == 0 && lane == 0) {
+        if (warp == 0) {
             // -------------------------------------------------------- producer
-            prefetch_tmap(&tm_q);
-            prefetch_tmap(&tm_k);
-            prefetch_tmap(&tm_v);
-            prefetch_tmap(&tm_do);
-            mbar_expect_tx(&S.kv_full, 2 * kTile);
-            tma_load_3d(S.k, &tm_k, &S.kv_full, 0, kvh, k_start + j0);
-            tma_load_3d(S.v, &tm_v, &S.kv_full, 0, kvh, k_start + j0);
-            int t = 0;
+            // (converged warp: every lane waits, lane 0 issues the copies)
+            if (lane == 0) {
+                prefetch_tmap(&tm_q);
+                prefetch_tmap(&tm_k);
+                prefetch_tmap(&tm_v);
+                prefetch_tmap(&tm_do);
+                mbar_expect_tx(&S.kv_full, 2 * kTile);
+                tma_load_3d(S.k, &tm_k, &S.kv_full, 0, kvh, k_start + j0);
+                tma_load_3d(S.v, &tm_v, &S.kv_full, 0, kvh, k_start + j0);
+            }
+            int t = 0, g_c = 0, qt_c = 0;
             for (; t < T; ++t) {
                 const int st = t % kQStages;
-                if (t >= kQStages && !mbar_wait(&S.qdo_empty[st], (t / kQStages - 1) & 1, abort)) break;
-                const int h = kvh * p.group + t / nqt;
-                const int q0 = (qr.lo + t % nqt) * BM;
-                mbar_expect_tx(&S.qdo_full[st], 2 * kTile);
-                tma_load_3d(S.q[st], &tm_q, &S.qdo_full[st], 0, h, q_start + q0);
-                tma_load_3d(S.dout[st], &tm_do, &S.qdo_full[st], 0, h, q_start + q0);
+                if (t >= kQStages &&
+                    !__all_sync(0xffffffffu, mbar_wait(&S.qdo_empty[st], (t / kQStages - 1) & 1, abort)))
+                    break;
+                if (lane == 0) {
+                    const int h = kvh * p.group + g_c;
+                    const int q0 = (qr.lo + qt_c) * BM;
+                    mbar_expect_tx(&S.qdo_full[st], 2 * kTile);
+                    tma_load_3d(S.q[st], &tm_q, &S.qdo_full[st], 0, h, q_start + q0);
+                    tma_load_3d(S.dout[st], &tm_do, &S.qdo_full[st], 0, h, q_start + q0);
+                }
+                if (++qt_c == nqt) {
+                    qt_c = 0;
+                    ++g_c;
+                }
             }
-            drain_wait(&S.kv_full, 0);
-            for (int st = 0; st < kQStages; ++st) {
-                const int n = t > st ? (t - st + kQStages - 1) / kQStages : 0;  // loads issued into stage st
-                if (n > 0) drain_wait(&S.qdo_full[st], (n - 1) & 1);
+            if (lane == 0) {
+                drain_wait(&S.kv_full, 0);
+                for (int st = 0; st < kQStages; ++st) {
+                    const int n = t > st ? (t - st + kQStages - 1) / kQStages : 0;  // loads issued into stage st
+                    if (n > 0) drain_wait(&S.qdo_full[st], (n - 1) & 1);
+                }
             }
-        } else if (warp == 2 && lane == 0 && T > 0) {
+            __syncwarp();
+        } else if (warp == 2 && T > 0) {
             // -------------------------------------------------------- dQ reducer
+            // (converged warp: every lane waits, lane 0 issues the reduce-adds)
             // Adds each staged dQ tile (two 32-column fp32 halves) to the fp32
             // accumulator with TMA bulk tensor reduce-adds, then frees the stage.
+            int g_c = 0, qt_c = 0;
             for (int tt = 0; tt < T; ++tt) {
-                if (!mbar_wait(&S.dq_staged, tt & 1, abort)) break;
-                const int hh = kvh * p.group + tt / nqt;
-                const int qq0 = (qr.lo + tt % nqt) * BM;
-                tma_reduce_add_3d(&tm_dq, S.dq_stage[0], 0, hh, q_start + qq0);
-                tma_reduce_add_3d(&tm_dq, S.dq_stage[1], 32, hh, q_start + qq0);
-                bulk_commit_group();
-                bulk_wait_read_all();
-                mbar_arrive(&S.dq_stage_free);
+                if (!__all_sync(0xffffffffu, mbar_wait(&S.dq_staged, tt & 1, abort))) break;
+                if (lane == 0) {
+                    const int hh = kvh * p.group + g_c;
+                    const int qq0 = (qr.lo + qt_c) * BM;
+                    tma_reduce_add_3d(&tm_dq, S.dq_stage[0], 0, hh, q_start + qq0);
+                    tma_reduce_add_3d(&tm_dq, S.dq_stage[1], 32, hh, q_start + qq0);
+                    bulk_commit_group();
+                    bulk_wait_read_all();
+                    mbar_arrive(&S.dq_stage_free);
+                }
+                __syncwarp();
+                if (++qt_c == nqt) {
+                    qt_c = 0;
+                    ++g_c;
+                }
             }
-            bulk_wait_all();  // the reduce-adds have landed before the CTA exits
+            if (lane == 0) bulk_wait_all();  // the reduce-adds have landed before the CTA exits
+            __syncwarp();
         } else if ((warp == 1 || warp == 3) && T > 0) {
             // -------------------------------------------------------- MMA issuers
             // Two issuing warps feed the tensor core independent instruction
