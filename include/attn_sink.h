@@ -230,6 +230,25 @@ int attn_sink_decode_paged_append(const attn_bf16* q, const attn_bf16* k_new, co
                                   float* lse, void* stream);
 
 /*
+ * attn_sink_fwd on HOST-resident tensors: the library copies each request's
+ * q / k / v rows to the device, runs the forward for that request and copies
+ * its out / lse rows back, pipelined on library-owned streams so that the copies
+ * of neighbouring requests overlap the kernel (same arithmetic and results as
+ * attn_sink_fwd).  All tensor arguments, cu_seqlens_q and cu_seqlens_k
+ * included, are host pointers; the layouts are those of attn_sink_fwd and the
+ * row counts come from cu_seqlens_*[batch].  Host buffers should be
+ * page-locked (cudaHostAlloc / cudaHostRegister) for the copies to overlap;
+ * pageable buffers still give correct results, without overlap.  Returns once
+ * the work is queued; `stream` waits for all of it (synchronise `stream`
+ * before reading out / lse).  Device scratch for the whole batch comes from the
+ * library's stream-ordered pool.  Supported: head_dim 64; hq % hkv == 0.
+ */
+int attn_sink_fwd_host(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v,
+                       const float* sink, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                       int batch, int hq, int hkv, int head_dim, int win_first, int win_last,
+                       int causal, float scale, attn_bf16* out, float* lse, void* stream);
+
+/*
  * Varlen extend / prefill whose keys and values live in a paged cache (the
  * serving extend path: sglang PR "openai oss attention sink support with
  * trtllm-gen backend", Highlights: the extend path passes sink=; the prefix is

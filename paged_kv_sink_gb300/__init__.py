@@ -13,6 +13,7 @@ from ._lib import (  # noqa: F401
     attn_sink_decode_paged_append,
     attn_sink_decode_paged_noalloc,
     attn_sink_fwd,
+    attn_sink_fwd_host,
     attn_sink_fwd_kvpacked,
     attn_sink_fwd_paged,
     attn_sink_fwd_qkvpacked,

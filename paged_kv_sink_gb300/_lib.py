@@ -32,6 +32,7 @@ _SIGS = {
                                        _P, _P],
     "attn_sink_bwd": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I,
                       _I, _F, _P, _P, _P, _P, _P],
+    "attn_sink_fwd_host": [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P],
     "attn_sink_fwd_strided": [_P, _P, _P, _L, _L, _L, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I,
                               _I, _F, _P, _P, _P],
     "attn_sink_bwd_strided": [_P, _P, _P, _L, _L, _L, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
@@ -125,6 +126,34 @@ def attn_sink_fwd(q, k, v, sink, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_s
                              d, int(max_seqlen_q), int(max_seqlen_k), int(win_first), int(win_last),
                              1 if causal else 0, float(scale), _ptr(out), _ptr(lse), _stream(stream))
     _check("attn_sink_fwd", rc)
+    return out, lse
+
+
+def attn_sink_fwd_host(q, k, v, sink, cu_seqlens_q, cu_seqlens_k, win_first=0, win_last=0, causal=True,
+                       scale=0.0, out=None, lse=None, return_lse=True, stream=None):
+    """attn_sink_fwd on host (CPU, preferably pinned) tensors: the library moves
+    each request's rows to the device and back, pipelined against the kernels.
+    Returns (out, lse) as host tensors; they are valid after ``stream`` (default:
+    the current CUDA stream) is synchronised."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, n, dev=False)
+    _need(sink, torch.float32, "sink", dev=False)
+    _need(cu_seqlens_q, torch.int32, "cu_seqlens_q", dev=False)
+    _need(cu_seqlens_k, torch.int32, "cu_seqlens_k", dev=False)
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (sink, "sink"), (cu_seqlens_q, "cu_seqlens_q"),
+                 (cu_seqlens_k, "cu_seqlens_k")):
+        if t is not None and t.is_cuda:
+            raise TypeError(f"{n} must be a host tensor")
+    tq, hq, d = q.shape
+    hkv = k.shape[1]
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    if lse is None and return_lse:
+        lse = torch.empty((hq, tq), dtype=torch.float32, pin_memory=True)
+    rc = lib().attn_sink_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(sink), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                                  cu_seqlens_q.numel() - 1, hq, hkv, d, int(win_first), int(win_last),
+                                  1 if causal else 0, float(scale), _ptr(out), _ptr(lse), _stream(stream))
+    _check("attn_sink_fwd_host", rc)
     return out, lse
 
 

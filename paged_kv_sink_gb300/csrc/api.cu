@@ -12,6 +12,7 @@
 #include "bwd.h"
 #include "common.cuh"
 #include "decode.h"
+#include "host_io.h"
 #include "kv_append.h"
 #include "prefill.h"
 
@@ -370,6 +371,54 @@ int attn_sink_fwd_strided(const attn_bf16* q, const attn_bf16* k, const attn_bf1
     return fwd_impl(q, k, v, q_row_stride, k_row_stride, v_row_stride, sink, cu_seqlens_q, cu_seqlens_k, batch,
                     total_q, total_k, hq, hkv, head_dim, max_seqlen_q, max_seqlen_k, win_first, win_last, causal,
                     scale, out, lse, stream);
+}
+
+int attn_sink_fwd_host(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, const float* sink,
+                       const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch, int hq, int hkv,
+                       int head_dim, int win_first, int win_last, int causal, float scale, attn_bf16* out,
+                       float* lse, void* stream) {
+    t_last_error.clear();
+    if (batch < 0 || hq <= 0 || hkv <= 0 || win_first < 0)
+        return fail(ATTN_SINK_ERR_INVALID, "fwd_host: sizes must be non-negative (heads positive)");
+    if (win_last > 0 && !causal)
+        return fail(ATTN_SINK_ERR_INVALID, "fwd_host: first/last-window selection needs causal attention");
+    if (head_dim != 64) return fail(ATTN_SINK_ERR_UNSUPPORTED, "fwd_host: head_dim %d not supported (64)", head_dim);
+    if (hq % hkv) return fail(ATTN_SINK_ERR_UNSUPPORTED, "fwd_host: hq %% hkv != 0");
+    if (batch == 0) return ATTN_SINK_OK;
+    if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_k || !out)
+        return fail(ATTN_SINK_ERR_INVALID, "fwd_host: NULL pointer");
+    if (cu_seqlens_q[0] != 0 || cu_seqlens_k[0] != 0)
+        return fail(ATTN_SINK_ERR_INVALID, "fwd_host: cu_seqlens must start at 0");
+    for (int b = 0; b < batch; ++b)
+        if (cu_seqlens_q[b + 1] < cu_seqlens_q[b] || cu_seqlens_k[b + 1] < cu_seqlens_k[b])
+            return fail(ATTN_SINK_ERR_INVALID, "fwd_host: cu_seqlens must be non-decreasing");
+    attn::hostio::Args a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.sink = sink;
+    a.cu_q = cu_seqlens_q;
+    a.cu_k = cu_seqlens_k;
+    a.out = out;
+    a.lse = lse;
+    a.batch = batch;
+    a.total_q = cu_seqlens_q[batch];
+    a.total_k = cu_seqlens_k[batch];
+    a.hq = hq;
+    a.hkv = hkv;
+    a.win_first = win_first;
+    a.win_last = win_last;
+    a.causal = causal ? 1 : 0;
+    a.scale = resolve_scale(scale, head_dim);
+    if (a.total_q == 0) return ATTN_SINK_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Scratch ws;
+    cudaError_t e = ws.alloc(attn::hostio::scratch_bytes(a), s);
+    if (e != cudaSuccess) return cuda_fail(e, "fwd_host: scratch allocation");
+    std::string err;
+    e = attn::hostio::run(a, ws.ptr, s, &err);
+    if (e != cudaSuccess) return fail(ATTN_SINK_ERR_CUDA, "fwd_host: %s: %s", err.c_str(), cudaGetErrorString(e));
+    return ATTN_SINK_OK;
 }
 
 int attn_sink_fwd_paged(const attn_bf16* q, const attn_bf16* k_new, const attn_bf16* v_new, attn_bf16* k_cache,
