@@ -39,8 +39,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel source it was measured on and is reported only while that source is
 # unchanged.
 NCU_TRAFFIC = {
-    # profiles/fwd_kernel_extend_varlen.md: 443.2 MB read + 259.3 MB written per launch
-    "fwd_kernel/extend_varlen": {"src": "5da617d4d921001f", "bytes": 702_455_552},
+    # profiles/fwd_kernel_extend_varlen.md: 442.5 MB read + 258.5 MB written per launch
+    "fwd_kernel/extend_varlen": {"src": "aefeee9909ec7232", "bytes": 701_026_304},
     # profiles/bwd_main_kernel_train.md: 2.594 GB read + 1.152 GB written per launch
     "bwd_main_kernel/train": {"src": "42e25632af854dce", "bytes": 3_745_681_000},
     # profiles/decode_split_kernel_decode_sink.md: decode_split_kernel, 1.944 GB + 0.011 GB

@@ -97,8 +97,10 @@ enum {
  *   win_first, win_last          window selection (needs causal = 1)
  *   out          (total_q, hq, head_dim) bf16
  *   lse          (hq, total_q) fp32, natural log, includes the sink; may be NULL
- * Supported: head_dim 64; hq % hkv == 0.  Key/value rows between requests
- * must be finite (a tile may read its neighbour's rows and mask them).
+ * Supported: head_dim 64; hq % hkv == 0.  A request's results depend on its
+ * own rows only: the value rows that its last key tile covers past its last
+ * key (another request's, or beyond cu_seqlens_k[batch]) are replaced by zeros
+ * in shared memory, so they may hold anything, NaN included.
  */
 int attn_sink_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v,
                   const float* sink, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
@@ -268,7 +270,9 @@ int attn_sink_fwd_host(const attn_bf16* q, const attn_bf16* k, const attn_bf16* 
  *   max_seqlen_q, max_seqlen_k   host upper bounds (grid sizing, append grid)
  *   sink, win_first, win_last, causal, scale, out, lse: as in attn_sink_fwd
  * Supported: head_dim 64; hq % hkv == 0; page_size a power of two >= 8
- * (a 128-key tile is then one TMA copy per page segment).
+ * (a 128-key tile is then one TMA copy per page segment).  Cache slots that a
+ * request does not own (the rest of its last page, any other page) never
+ * reach its results and may hold anything, NaN included.
  */
 int attn_sink_fwd_paged(const attn_bf16* q, const attn_bf16* k_new, const attn_bf16* v_new,
                         attn_bf16* k_cache, attn_bf16* v_cache, const int32_t* page_table,
@@ -292,7 +296,10 @@ int attn_sink_fwd_paged(const attn_bf16* q, const attn_bf16* k_new, const attn_b
  *                of each KV head)
  *   dsink        (hq,) fp32; must be non-NULL iff sink is non-NULL; written
  *                (not accumulated)
- * Supported: head_dim 64; hq % hkv == 0.
+ * Supported: head_dim 64; hq % hkv == 0.  A tile that reaches past a
+ * request's last query or key row reads the next request's rows (rows past
+ * total_q / total_k read as zeros) and gives them zero weight: they must be
+ * finite, and then have no effect.
  */
 int attn_sink_bwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, const float* sink,
                   const attn_bf16* out, const float* lse, const attn_bf16* dout,

@@ -150,8 +150,10 @@ cudaError_t run(const Args& a, void* dev_buf, cudaStream_t caller, std::string* 
         f.out = dout;
         f.lse = a.lse ? dlse : nullptr;
         f.batch = 1;
-        f.total_q = a.total_q;
-        f.total_k = a.total_k;
+        f.total_q = a.total_q;  // also the lse head stride
+        // K/V rows past this request are out of the tensor for this launch (the
+        // copy engine may still be writing them): the tail tile reads zeros.
+        f.total_k = k1;
         f.hq = a.hq;
         f.hkv = a.hkv;
         f.head_dim = 64;

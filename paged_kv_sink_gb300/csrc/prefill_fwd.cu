@@ -67,6 +67,7 @@ struct __align__(1024) Smem {
     uint64_t v_full[VSTAGE], v_empty[VSTAGE];
     uint64_t s_full, s_free, p_full, o_done;  // one phase per key tile
     uint64_t final_bar;
+    uint64_t v_tail;  // the V tile that holds the request's last key lands here first
     uint32_t tmem_base;
     int abort;
 };
@@ -164,6 +165,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         mbar_init(&S.p_full, 128);
         mbar_init(&S.o_done, 1);
         mbar_init(&S.final_bar, 1);
+        mbar_init(&S.v_tail, 1);
         S.abort = 0;
         fence_mbar_init();
     }
@@ -199,16 +201,24 @@ __global__ void __launch_bounds__(kThreads, 2)
                     tma_load_3d(S.q, &tm_q, &S.q_full, 0, h, q_start + qs);
                 }
             }
+            // The one V tile that reaches past the request's last key (rows of the
+            // next request, of no request, or unwritten cache slots) lands on v_tail;
+            // this warp then zeroes those rows before it releases the stage, so they
+            // enter P V as exact zeros whatever the memory held (a masked P of 0
+            // times a NaN or an infinity would not vanish).
+            bool tail_issued = false;
             int it = 0;
             for (; it < ntiles; ++it) {
                 const int st = it % nst;
                 if (it >= nst && !__all_sync(0xffffffffu, mbar_wait(&empty[st], ((it / nst) - 1) & 1, abort)))
                     break;
                 const int t = it < ta ? it : tb + (it - ta);
+                const bool tail = !is_k && (t + 1) * BN > Lk;
+                uint64_t* bar = tail ? &S.v_tail : &full[st];
                 if (!paged) {
                     if (lane == 0) {
-                        mbar_expect_tx(&full[st], kTile);
-                        tma_load_3d(dst0 + st * kTile, tm, &full[st], 0, kvh, k_start + t * BN);
+                        mbar_expect_tx(bar, kTile);
+                        tma_load_3d(dst0 + st * kTile, tm, bar, 0, kvh, k_start + t * BN);
                     }
                 } else {
                     // Segment `lane` covers keys j .. j + (1 << seg_shift) - 1, inside one page.
@@ -222,18 +232,32 @@ __global__ void __launch_bounds__(kThreads, 2)
                         else
                             raise_status(ATTN_SINK_DEV_PAGE_OOB);
                     }
-                    if (lane == 0) mbar_expect_tx(&full[st], kTile);
+                    if (lane == 0) mbar_expect_tx(bar, kTile);
                     for (int sg = 0; sg < nseg; ++sg) {
                         const int sl = __shfl_sync(0xffffffffu, slot, sg);
                         if (lane == 0)
-                            tma_load_3d(dst0 + st * kTile + ((uint32_t)sg << p.seg_shift) * 128u, tm, &full[st], 0,
-                                        kvh, sl);
+                            tma_load_3d(dst0 + st * kTile + ((uint32_t)sg << p.seg_shift) * 128u, tm, bar, 0, kvh,
+                                        sl);
                     }
+                }
+                if (tail) {
+                    // Used once per CTA (one tile holds the last key): parity 0.
+                    tail_issued = true;
+                    if (!__all_sync(0xffffffffu, mbar_wait(&S.v_tail, 0, abort))) break;
+                    // Key row r is the 128 bytes at r * 128 (the swizzle permutes
+                    // 16-byte chunks within a row), so rows Lk - t*BN .. BN - 1 are
+                    // one contiguous range.
+                    uint4* vt = reinterpret_cast<uint4*>(dst0 + st * kTile);
+                    for (int c = (Lk - t * BN) * 8 + lane; c < BN * 8; c += 32) vt[c] = make_uint4(0u, 0u, 0u, 0u);
+                    fence_proxy_async_smem();  // the tensor core reads the zeros through the async proxy
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&full[st]);
                 }
             }
             // Drain: every copy issued must have landed before the CTA exits.
             if (lane == 0) {
                 if (is_k) drain_wait(&S.q_full, 0);
+                if (tail_issued) drain_wait(&S.v_tail, 0);
                 for (int st = 0; st < nst; ++st) {
                     const int n = it > st ? (it - st + nst - 1) / nst : 0;
                     if (n > 0) drain_wait(&full[st], (n - 1) & 1);

@@ -1,0 +1,81 @@
+"""Rows that a request's last key tile covers past its own keys must not reach its
+output: with NaN in every cache slot no request owns, and NaN in a neighbouring
+request's rows and past the end of the K/V buffers, the forward's outputs equal
+those of the clean inputs bit for bit."""
+import pytest
+import torch
+
+from oracle import attn_sink_oracle as orc
+from paged_kv_sink_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ext():
+    from paged_kv_sink_gb300 import build
+    build.build()
+    import paged_kv_sink_gb300 as ext
+    return ext
+
+
+def _owned_slots(page_table, seqlens_k, page_size, num_slots):
+    owned = torch.zeros(num_slots, dtype=torch.bool)
+    for b, L in enumerate(seqlens_k.tolist()):
+        for t in range(L):
+            owned[int(page_table[b, t // page_size]) * page_size + t % page_size] = True
+    return owned
+
+
+@pytest.mark.parametrize("page_size,win", [(16, (0, 0)), (8, (16, 200)), (128, (0, 0))])
+def test_fwd_paged_ignores_unowned_slots(ext, page_size, win):
+    pe = wl.make_paged_extend(seqlens_q=[77, 1, 130], seqlens_k=[301, 45, 130], hq=8, hkv=2, d=64,
+                              page_size=page_size, win_first=win[0], win_last=win[1], seed=17, extra_pages=4)
+    kw, vw = orc.kv_append(pe.k_cache, pe.v_cache, pe.page_table, pe.seqlens_k, pe.k_new, pe.v_new, page_size,
+                           cu_new=pe.cu_seqlens_q)
+    n_slots = kw.shape[0] * page_size
+    owned = _owned_slots(pe.page_table, pe.seqlens_k, page_size, n_slots)
+    assert not owned.all()
+    dev = "cuda"
+    results = []
+    for poison in (False, True):
+        kc, vc = kw.clone().view(n_slots, -1), vw.clone().view(n_slots, -1)
+        if poison:
+            kc[~owned] = float("nan")
+            vc[~owned] = float("nan")
+        out, lse = ext.attn_sink_fwd_paged(pe.q.to(dev), kc.view_as(kw).to(dev), vc.view_as(vw).to(dev),
+                                           pe.page_table.to(dev), pe.cu_seqlens_q.to(dev), pe.seqlens_k.to(dev),
+                                           pe.max_seqlen_q, pe.max_seqlen_k, pe.sink.to(dev),
+                                           win_first=win[0], win_last=win[1])
+        torch.cuda.synchronize()
+        assert ext.device_status() == 0
+        results.append((out.cpu(), lse.cpu()))
+    assert not results[0][0].isnan().any()
+    assert torch.equal(results[0][0], results[1][0])
+    assert torch.equal(results[0][1], results[1][1])
+
+
+def test_fwd_neighbour_and_trailing_rows_do_not_leak(ext):
+    p = wl.make_prefill(seqlens_q=[100, 77, 129], seqlens_k=[300, 200, 129], hq=8, hkv=2, d=64, sink="normal",
+                        seed=23)
+    cq, ck = p.cu_seqlens_q.tolist(), p.cu_seqlens_k.tolist()
+    dev = "cuda"
+    results = []
+    for poison in (False, True):
+        q, k, v = p.q.clone(), p.k.clone(), p.v.clone()
+        if poison:
+            # request 1 holds NaN in every row, and the K/V buffers run 64 NaN rows past the last key
+            q[cq[1]:cq[2]] = float("nan")
+            k[ck[1]:ck[2]] = float("nan")
+            v[ck[1]:ck[2]] = float("nan")
+            pad = torch.full((64,) + tuple(k.shape[1:]), float("nan"), dtype=k.dtype)
+            k, v = torch.cat([k, pad]), torch.cat([v, pad])
+        out, lse = ext.attn_sink_fwd(q.to(dev), k.to(dev), v.to(dev), p.sink.to(dev), p.cu_seqlens_q.to(dev),
+                                     p.cu_seqlens_k.to(dev), p.max_seqlen_q, p.max_seqlen_k)
+        torch.cuda.synchronize()
+        assert ext.device_status() == 0
+        results.append((out.cpu(), lse.cpu()))
+    for lo, hi in ((cq[0], cq[1]), (cq[2], cq[3])):
+        assert not results[0][0][lo:hi].isnan().any()
+        assert torch.equal(results[0][0][lo:hi], results[1][0][lo:hi])
+        assert torch.equal(results[0][1][:, lo:hi], results[1][1][:, lo:hi])
