@@ -72,3 +72,63 @@ def test_validation_without_gpu(lib):
     rc = lib.attn_sink_decode_paged(None, None, None, None, 4, None, 0, 8, 2, 64, 16, 4, None, 0, 0, 0.0,
                                     None, None, None)
     assert rc == 0
+
+
+def test_validation_of_the_extended_entry_points_without_gpu(lib):
+    """Host-side checks of the strided, paged, append and host-buffer entry points
+    return their status codes before any CUDA call."""
+    P = ctypes.c_void_p(16)  # never dereferenced: validation fails first
+    # strided forward: a q row stride below heads*64, and one that breaks 16-byte rows
+    for q_rs in (200, 260):
+        rc = lib.attn_sink_fwd_strided(P, P, P, q_rs, 0, 0, None, P, P, 1, 8, 8, 4, 2, 64, 8, 8, 0, 0, 1, 0.0,
+                                       P, None, None)
+        assert rc == -1
+        assert b"row stride" in lib.attn_sink_last_error()
+    # strided backward: bad k stride
+    rc = lib.attn_sink_bwd_strided(P, P, P, 0, 100, 0, None, P, P, P, P, P, 1, 8, 8, 4, 2, 64, 8, 8, 0, 0, 1,
+                                   0.0, P, P, P, 0, 0, 0, None, None)
+    assert rc == -1
+    assert b"k row stride" in lib.attn_sink_last_error()
+    # paged forward: page size not a power of two >= 8; k_new without v_new
+    for ps in (24, 4):
+        rc = lib.attn_sink_fwd_paged(P, None, None, P, P, P, 4, P, P, 1, 8, 4, 2, 64, ps, 16, 8, 40, None, 0, 0,
+                                     1, 0.0, P, None, None)
+        assert rc == -2
+    rc = lib.attn_sink_fwd_paged(P, P, None, P, P, P, 4, P, P, 1, 8, 4, 2, 64, 16, 16, 8, 40, None, 0, 0, 1,
+                                 0.0, P, None, None)
+    assert rc == -1
+    assert b"together" in lib.attn_sink_last_error()
+    # paged forward: windows need causal attention
+    rc = lib.attn_sink_fwd_paged(P, None, None, P, P, P, 4, P, P, 1, 8, 4, 2, 64, 16, 16, 8, 40, None, 4, 8, 0,
+                                 0.0, P, None, None)
+    assert rc == -1
+    # append: head_dim 96; several rows per request without cu_new; misaligned cache; empty is a no-op
+    rc = lib.attn_sink_kv_append(P, P, P, P, P, 4, 2, 2, 96, 16, 8, 3, P, P, None)
+    assert rc == -2
+    rc = lib.attn_sink_kv_append(P, P, None, P, P, 4, 2, 2, 64, 16, 8, 3, P, P, None)
+    assert rc == -1
+    assert b"cu_new" in lib.attn_sink_last_error()
+    rc = lib.attn_sink_kv_append(P, P, P, P, P, 4, 2, 2, 64, 16, 8, 3, ctypes.c_void_p(24), P, None)
+    assert rc == -1
+    assert b"aligned" in lib.attn_sink_last_error()
+    rc = lib.attn_sink_kv_append(None, None, None, None, None, 4, 0, 2, 64, 16, 8, 0, None, None, None)
+    assert rc == 0
+    # decode with append: NULL new rows
+    rc = lib.attn_sink_decode_paged_append(P, None, None, P, P, P, 4, P, 2, 8, 2, 64, 16, 4, None, 0, 0, 0.0,
+                                           P, None, None)
+    assert rc == -1
+    assert b"k_new" in lib.attn_sink_last_error()
+    # host-buffer forward: cu_seqlens are read on the host and checked there
+    def fwd_host(cu_q, cu_k, batch, head_dim=64):
+        aq = (ctypes.c_int32 * len(cu_q))(*cu_q)
+        ak = (ctypes.c_int32 * len(cu_k))(*cu_k)
+        return lib.attn_sink_fwd_host(P, P, P, None, ctypes.cast(aq, ctypes.c_void_p),
+                                      ctypes.cast(ak, ctypes.c_void_p), batch, 4, 2, head_dim, 0, 0, 1, 0.0, P,
+                                      None, None)
+    assert fwd_host([1, 5], [0, 5], 1) == -1
+    assert b"start at 0" in lib.attn_sink_last_error()
+    assert fwd_host([0, 5, 3], [0, 5, 9], 2) == -1
+    assert b"non-decreasing" in lib.attn_sink_last_error()
+    assert fwd_host([0, 5], [0, 5], 1, head_dim=128) == -2
+    assert fwd_host([0], [0], 0) == 0
+    assert fwd_host([0, 0, 0], [0, 7, 9], 2) == 0  # no query rows: nothing to do
