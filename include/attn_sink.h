@@ -359,6 +359,18 @@ int attn_sink_visible_slots(const int32_t* seqlens, const int32_t* page_table, i
  */
 int attn_sink_device_status(void* stream);
 
+/*
+ * Self-test of the bounded wait behind every pipeline barrier of the kernels
+ * (no counterpart on the pages: it is how a stalled pipeline is detected).
+ * Launches one single-thread kernel on `stream` that waits on an mbarrier of
+ * its own.  complete != 0: the barrier's phase is completed first and the wait
+ * returns at once (no status).  complete == 0: nothing arrives, the wait gives
+ * up after its time limit (1 s), sets ATTN_SINK_DEV_TIMEOUT and the kernel
+ * returns; the context stays usable.  Asynchronous; returns ATTN_SINK_OK or
+ * ATTN_SINK_ERR_CUDA (launch failure).
+ */
+int attn_sink_selftest_wait(int complete, void* stream);
+
 /* Text of the calling thread's last failure ("" if none).  Never NULL. */
 const char* attn_sink_last_error(void);
 

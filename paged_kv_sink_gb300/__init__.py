@@ -18,6 +18,7 @@ from ._lib import (  # noqa: F401
     attn_sink_fwd_paged,
     attn_sink_fwd_qkvpacked,
     attn_sink_kv_append,
+    attn_sink_selftest_wait,
     attn_sink_visible_ranges,
     attn_sink_visible_slots,
     device_status,

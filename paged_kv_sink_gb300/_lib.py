@@ -45,6 +45,7 @@ _SIGS = {
     "attn_sink_visible_ranges": [_P, _I, _I, _I, _P, _P],
     "attn_sink_visible_slots": [_P, _P, _I, _I, _I, _I, _I, _I, _P, _I, _P],
     "attn_sink_device_status": [_P],
+    "attn_sink_selftest_wait": [_I, _P],
     "attn_sink_last_error": [],
     "attn_sink_version": [],
 }
@@ -394,6 +395,13 @@ def attn_sink_visible_slots(seqlens, page_table, page_size, num_pages, win_first
                                        _stream(stream))
     _check("attn_sink_visible_slots", rc)
     return slots
+
+
+def attn_sink_selftest_wait(complete, stream=None):
+    """One single-thread kernel waits on an mbarrier: completed first (returns at
+    once) or never completed (gives up after the wait limit and sets DEV_TIMEOUT,
+    read by device_status)."""
+    _check("attn_sink_selftest_wait", lib().attn_sink_selftest_wait(1 if complete else 0, _stream(stream)))
 
 
 def device_status(stream=None) -> int:

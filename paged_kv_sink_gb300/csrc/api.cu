@@ -14,6 +14,7 @@
 #include "decode.h"
 #include "host_io.h"
 #include "kv_append.h"
+#include "selftest.h"
 #include "prefill.h"
 
 namespace {
@@ -593,8 +594,16 @@ int attn_sink_device_status(void* stream) {
     if (!e) e = attn::prefill::status_exchange(s, &bits);
     if (!e) e = attn::bwd::status_exchange(s, &bits);
     if (!e) e = attn::kvappend::status_exchange(s, &bits);
+    if (!e) e = attn::selftest::status_exchange(s, &bits);
     if (e) return cuda_fail(static_cast<cudaError_t>(e), "device_status");
     return bits;
+}
+
+int attn_sink_selftest_wait(int complete, void* stream) {
+    t_last_error.clear();
+    cudaError_t e = attn::selftest::launch_wait(complete, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "selftest_wait: launch");
+    return ATTN_SINK_OK;
 }
 
 }  // extern "C"
