@@ -184,9 +184,18 @@ def max_over_ranks(torch, dist, values, device="cpu"):
     return [float(v) for v in t.tolist()]
 
 
-def job_rate(work_per_rank, world, seconds_max):
+def sum_over_ranks(torch, dist, value, device="cpu"):
+    """Sum of a per-rank value over all ranks (identity at N = 1)."""
+    if dist is None:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def job_rate(work_all_ranks, seconds_max):
     """Whole-job throughput: the work all ranks did over the slowest rank's time."""
-    return work_per_rank * world / seconds_max
+    return work_all_ranks / seconds_max
 
 
 def rank_sync(torch, dist):
@@ -521,7 +530,7 @@ def main():
     flush = _flush_buf(torch, dev)
 
     if args.only:
-        w = wl.workload("decode_sink" if args.only == "decode_append" else args.only, seed=rank)
+        w = wl.workload("decode_sink" if args.only == "decode_append" else args.only, seed=0)
         if args.only == "train":
             r = bench_train(torch, ext, dev, w, args.steps, args.warmup, flush, peaks, peak_src)
         elif args.only == "extend_paged":
@@ -534,7 +543,8 @@ def main():
             print(json.dumps({"workload": w.name, **r}))
         return
 
-    p = wl.workload(args.workload, seed=rank)
+    # Every rank runs the same seeded workload: N replicas with fixed work per GPU.
+    p = wl.workload(args.workload, seed=0)
     with ClockSampler(local) as clk:
         ms, flops, roof, times = bench_extend(torch, ext, dev, p, args.steps, args.warmup, flush, peaks,
                                               peak_src, sync=lambda: rank_sync(torch, dist))
@@ -542,27 +552,28 @@ def main():
     e2e_ms, h2d, d2h = e2e_extend(torch, ext, dev, p, max(3, args.steps // 4), 2)
 
     ms_max, e2e_ms = max_over_ranks(torch, dist, [ms, e2e_ms], device=dev)
-    value = job_rate(flops, world, ms_max * 1e-3) / 1e12
-    e2e_value = job_rate(flops, world, e2e_ms * 1e-3) / 1e12
+    flops_all = sum_over_ranks(torch, dist, flops, device=dev)
+    value = job_rate(flops_all, ms_max * 1e-3) / 1e12
+    e2e_value = job_rate(flops_all, e2e_ms * 1e-3) / 1e12
 
     extra = {}
     if not args.no_extra:
         for name in ("decode_sink", "decode_window"):
-            dc = wl.workload(name, seed=rank)
+            dc = wl.workload(name, seed=0)
             r = bench_decode(torch, ext, dev, dc, args.steps, args.warmup, flush, peaks, peak_src)
             if rank == 0 and not args.no_cpu and world == 1:
                 r["cpu_baseline"] = cpu_baseline_decode(dc)
             extra[name] = r
             del dc
-        tr = wl.workload("train", seed=rank)
+        tr = wl.workload("train", seed=0)
         extra["train"] = bench_train(torch, ext, dev, tr, max(3, args.steps // 2), args.warmup, flush, peaks,
                                      peak_src)
         del tr
-        pe = wl.workload("extend_paged", seed=rank)
+        pe = wl.workload("extend_paged", seed=0)
         extra["extend_paged"] = bench_extend_paged(torch, ext, dev, pe, max(3, args.steps // 2), args.warmup,
                                                    flush, peaks, peak_src)
         del pe
-        dc = wl.workload("decode_sink", seed=rank)
+        dc = wl.workload("decode_sink", seed=0)
         extra["decode_sink_append"] = bench_decode_append(torch, ext, dev, dc, args.steps, args.warmup, flush,
                                                           peaks, peak_src)
         del dc

@@ -29,8 +29,9 @@ def _worker(rank, world, port, q):
     try:
         mine = [1.0 + rank, 10.0 - rank]  # per-rank (ms, e2e ms)
         got = bench.max_over_ranks(torch, dist, mine)
+        work = bench.sum_over_ranks(torch, dist, 2.0e12 + 1.0e12 * rank)  # per-rank FLOPs
         dist.barrier()
-        q.put((rank, got, bench.job_rate(2.0e12, world, got[0] * 1e-3)))
+        q.put((rank, got, work, bench.job_rate(work, got[0] * 1e-3)))
     finally:
         dist.destroy_process_group()
 
@@ -42,19 +43,21 @@ def test_max_over_ranks_and_job_rate_gloo_world2():
     procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
     for p in procs:
         p.start()
-    res = dict((r, (g, v)) for r, g, v in (q.get(timeout=120) for _ in range(world)))
+    res = dict((r, (g, w, v)) for r, g, w, v in (q.get(timeout=120) for _ in range(world)))
     for p in procs:
         p.join(timeout=120)
         assert p.exitcode == 0
     for r in range(world):
-        got, rate = res[r]
+        got, work, rate = res[r]
         assert got == [2.0, 10.0]  # max of (1, 2) and (10, 9)
-        assert rate == pytest.approx(2.0e12 * 2 / 2.0e-3)
+        assert work == 5.0e12  # 2e12 + 3e12: every rank's own work, summed
+        assert rate == pytest.approx(5.0e12 / 2.0e-3)
 
 
 def test_single_rank_is_identity():
     assert bench.max_over_ranks(torch, None, [3, 4.5]) == [3.0, 4.5]
-    assert bench.job_rate(1.0, 1, 0.5) == 2.0
+    assert bench.sum_over_ranks(torch, None, 3) == 3.0
+    assert bench.job_rate(1.0, 0.5) == 2.0
 
 
 def test_reference_arm_under_torchrun_world2():
