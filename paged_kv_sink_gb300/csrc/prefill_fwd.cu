@@ -29,6 +29,8 @@
 // below 2^64, far inside fp32/bf16 range, so the result is exact.
 #include <cudaTypedefs.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "prefill.h"
 #include "sm103.cuh"
@@ -340,38 +342,48 @@ __global__ void __launch_bounds__(kThreads, 2)
                 break;
             }
             tc_fence_after();
+            // S arrives in two halves: the first 64 columns are waited for, the
+            // second half's load stays in flight while the first is exponentiated,
+            // and the first half of P is stored while the second is computed, so
+            // the TMEM load and store latencies overlap the exp2 work.
             uint32_t s[4][32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
+            tmem_ld32(tS, s[0]);
+            tmem_ld32(tS + 32, s[1]);
             tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(&S.s_free);
+            tmem_ld32(tS + 64, s[2]);
+            tmem_ld32(tS + 96, s[3]);
 
             const int jmax = j0 + BN - 1;
             const bool full = (!p.causal || jmax <= P0) && (jmax < Lk) &&
                               (p.win_last <= 0 || jmax < p.win_first || j0 >= P1 + 1 - p.win_last);
+            int c_hi = BN, f_hi = BN, w_lo = 0;
             if (!full) {
-                int c_hi = p.causal ? pos - j0 + 1 : BN;
+                c_hi = p.causal ? pos - j0 + 1 : BN;
                 c_hi = min(c_hi, Lk - j0);
-                const int f_hi = p.win_last > 0 ? p.win_first - j0 : BN;
-                const int w_lo = p.win_last > 0 ? pos + 1 - p.win_last - j0 : 0;
+                f_hi = p.win_last > 0 ? p.win_first - j0 : BN;
+                w_lo = p.win_last > 0 ? pos + 1 - p.win_last - j0 : 0;
+            }
+            // Hidden keys of columns 64*hf .. 64*hf + 63 become -inf.
+            auto mask_half = [&](auto hfc) {
+                constexpr int hf = decltype(hfc)::value;
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
+                for (int c = 2 * hf; c < 2 * hf + 2; ++c)
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int cc = c * 32 + i;
                         const bool vis = cc < c_hi && (cc < f_hi || cc >= w_lo);
                         if (!vis) s[c][i] = __float_as_uint(-INFINITY);
                     }
-            }
-            // P = 2^(s*scale*log2e - m_use) into registers (packed fp32x2 FMA, MUFU ex2,
-            // packed partial sums) before waiting for the previous P V.
+            };
+            // P = 2^(s*scale*log2e - m_use) of one half into w[32*hf ..] (packed fp32x2
+            // FMA, MUFU ex2, packed partial sums); returns the half's row sum.
             uint32_t w[64];
-            auto exps = [&](float m_use) -> float {
+            auto exps_half = [&](auto hfc, float m_use) -> float {
+                constexpr int hf = decltype(hfc)::value;
                 const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(-m_use, -m_use);
                 uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-                for (int e = 0; e < 64; ++e) {
+                for (int e = 32 * hf; e < 32 * hf + 32; ++e) {
                     const int i0 = 2 * e;
                     const uint64_t y = f2_fma(f2_pack(__uint_as_float(s[i0 >> 5][i0 & 31]),
                                                       __uint_as_float(s[(i0 + 1) >> 5][(i0 + 1) & 31])),
@@ -391,51 +403,78 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 return sum;
             };
+            using H0 = std::integral_constant<int, 0>;
+            using H1 = std::integral_constant<int, 1>;
+            // The previous P V must be complete before P is overwritten or O
+            // rescaled; it normally finished while this tile's S was computed.
+            auto wait_prev_pv = [&]() -> bool {
+                if (it == 0) return true;
+                const bool done = __all_sync(0xffffffffu, mbar_wait(&S.o_done, (it - 1) & 1, abort));
+                if (done) tc_fence_after();
+                return done;
+            };
             // Fast path: exponentiate against the current reference without the row
-            // max.  Every value is then <= 2^64 unless the row sum exceeds 2^64 (or
-            // overflowed), in which case the exact pass redoes the tile.
-            bool resc = false;
-            float alpha = 1.f;
-            float rs = 0.f;
+            // max.  Every value is then <= 2^64 unless a half's row sum exceeds 2^64
+            // (or overflowed), in which case the exact pass redoes the tile.
             bool slow = __any_sync(0xffffffffu, m_ref == -INFINITY);
-#pragma unroll 1
-            for (int pass = slow ? 1 : 0; pass < 2; ++pass) {
-                if (pass == 1) {
-                    // Row max: eight independent 3-input max chains of 16 values.
-                    float mc[8];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const uint32_t* v = &s[k >> 1][(k & 1) * 16];
-                        float m = max3f(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
-#pragma unroll
-                        for (int i = 3; i < 15; i += 2)
-                            m = max3f(m, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
-                        mc[k] = fmaxf(m, __uint_as_float(v[15]));
-                    }
-                    const float mx =
-                        max3f(max3f(mc[0], mc[1], mc[2]), max3f(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
-                    const float m_new = fmaxf(m_ref, mx * sl2);
-                    resc = m_new > m_ref + kRescaleThreshold;
-                    alpha = resc ? fast_exp2(m_ref - m_new) : 1.f;
-                    if (resc) {
-                        l *= alpha;
-                        m_ref = m_new;
-                    }
-                }
-                rs = exps(m_ref == -INFINITY ? 0.f : m_ref);
-                if (pass == 0 && !__any_sync(0xffffffffu, !(rs <= kFastSumLimit))) break;
-            }
-            l += rs;
-            if (it > 0) {
-                // The previous P V must be complete: it reads P in TMEM and
-                // accumulates into the O that a rescale touches.
-                ok = mbar_wait(&S.o_done, (it - 1) & 1, abort);
-                if (!__all_sync(0xffffffffu, ok)) {
-                    ok = false;
+            bool stored0 = false;
+            float rs = 0.f;
+            if (!slow) {
+                if (!full) mask_half(H0{});
+                const float rs0 = exps_half(H0{}, m_ref);
+                const bool ok0 = !__any_sync(0xffffffffu, !(rs0 <= kFastSumLimit));
+                if (!(ok = wait_prev_pv())) {
+                    tmem_ld_wait();
                     break;
                 }
-                tc_fence_after();
-                if (__any_sync(0xffffffffu, resc)) {
+                if (ok0) {
+                    tmem_st32(tP, *reinterpret_cast<uint32_t(*)[32]>(&w[0]));
+                    stored0 = true;
+                }
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(&S.s_free);
+                if (!full) mask_half(H1{});
+                const float rs1 = exps_half(H1{}, m_ref);
+                const bool ok1 = !__any_sync(0xffffffffu, !(rs1 <= kFastSumLimit));
+                if (ok0 && ok1) {
+                    rs = rs0 + rs1;
+                    tmem_st32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&w[32]));
+                } else {
+                    slow = true;
+                }
+            } else {
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(&S.s_free);
+                if (!full) {
+                    mask_half(H0{});
+                    mask_half(H1{});
+                }
+                if (!(ok = wait_prev_pv())) break;
+            }
+            if (slow) {
+                // Row max: eight independent 3-input max chains of 16 values.
+                float mc[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t* v = &s[k >> 1][(k & 1) * 16];
+                    float m = max3f(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+#pragma unroll
+                    for (int i = 3; i < 15; i += 2) m = max3f(m, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+                    mc[k] = fmaxf(m, __uint_as_float(v[15]));
+                }
+                const float mx = max3f(max3f(mc[0], mc[1], mc[2]), max3f(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
+                const float m_new = fmaxf(m_ref, mx * sl2);
+                const bool resc = m_new > m_ref + kRescaleThreshold;
+                const float alpha = resc ? fast_exp2(m_ref - m_new) : 1.f;
+                if (resc) {
+                    l *= alpha;
+                    m_ref = m_new;
+                }
+                const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+                rs = exps_half(H0{}, m_use) + exps_half(H1{}, m_use);
+                if (it > 0 && __any_sync(0xffffffffu, resc)) {
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         uint32_t o[32];
@@ -446,10 +485,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                         tmem_st32(tO + half * 32, o);
                     }
                 }
+                if (stored0) tmem_st_wait();  // the first half's earlier store lands before its rewrite
+                // P as bf16 pairs: TMEM column c holds keys 2c (low half) and 2c+1.
+                tmem_st32(tP, *reinterpret_cast<uint32_t(*)[32]>(&w[0]));
+                tmem_st32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&w[32]));
             }
-            // P as bf16 pairs: TMEM column c holds keys 2c (low half) and 2c+1.
-            tmem_st32(tP, *reinterpret_cast<uint32_t(*)[32]>(&w[0]));
-            tmem_st32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&w[32]));
+            l += rs;
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&S.p_full);
