@@ -342,16 +342,16 @@ __global__ void __launch_bounds__(kThreads, 2)
                 break;
             }
             tc_fence_after();
-            // S arrives in two halves: the first 64 columns are waited for, the
-            // second half's load stays in flight while the first is exponentiated,
-            // and the first half of P is stored while the second is computed, so
-            // the TMEM load and store latencies overlap the exp2 work.
+            // S is read into registers and released at once, so the next S runs on
+            // the tensor core during this tile's whole exp2 phase; P is computed and
+            // stored in two halves, the first half's TMEM store overlapping the
+            // second half's exp2 work.
             uint32_t s[4][32];
-            tmem_ld32(tS, s[0]);
-            tmem_ld32(tS + 32, s[1]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
             tmem_ld_wait();
-            tmem_ld32(tS + 64, s[2]);
-            tmem_ld32(tS + 96, s[3]);
+            tc_fence_before();
+            mbar_arrive(&S.s_free);
 
             const int jmax = j0 + BN - 1;
             const bool full = (!p.causal || jmax <= P0) && (jmax < Lk) &&
@@ -423,17 +423,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (!full) mask_half(H0{});
                 const float rs0 = exps_half(H0{}, m_ref);
                 const bool ok0 = !__any_sync(0xffffffffu, !(rs0 <= kFastSumLimit));
-                if (!(ok = wait_prev_pv())) {
-                    tmem_ld_wait();
-                    break;
-                }
+                if (!(ok = wait_prev_pv())) break;
                 if (ok0) {
                     tmem_st32(tP, *reinterpret_cast<uint32_t(*)[32]>(&w[0]));
                     stored0 = true;
                 }
-                tmem_ld_wait();
-                tc_fence_before();
-                mbar_arrive(&S.s_free);
                 if (!full) mask_half(H1{});
                 const float rs1 = exps_half(H1{}, m_ref);
                 const bool ok1 = !__any_sync(0xffffffffu, !(rs1 <= kFastSumLimit));
@@ -444,9 +438,6 @@ __global__ void __launch_bounds__(kThreads, 2)
                     slow = true;
                 }
             } else {
-                tmem_ld_wait();
-                tc_fence_before();
-                mbar_arrive(&S.s_free);
                 if (!full) {
                     mask_half(H0{});
                     mask_half(H1{});
