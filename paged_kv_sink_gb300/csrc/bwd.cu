@@ -15,7 +15,7 @@
 //    that see its keys.  Per step five tcgen05 GEMMs:
 //        S = Q K^T, dP = dO V^T              (TMEM, 128 x 128 fp32 each)
 //        dV += P^T dO, dK += dS^T Q          (TMEM accumulators over the whole loop)
-//        dQ  = dS K                          (TMEM, double-buffered)
+//        dQ  = dS K                          (TMEM; A = dS read from TMEM)
 //    Two warpgroups share the elementwise work: thread = (query row, half of the
 //    128 key columns), so the row's LSE and D are per-thread scalars.  They
 //    write P and scale dS to shared memory in the 128-byte-swizzled layout (read
@@ -44,8 +44,10 @@ constexpr int kWork = 256;      // elementwise threads: warps 4..11
 constexpr int kQStages = 3;     // Q / dO ring depth
 constexpr uint32_t kTile = 128 * 128;
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns
-constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDK = 320, cDQ = 384;  // dQ: 384, 448
+// TMEM columns: S, dP (fp32), dV, dK (fp32 accumulators over the whole loop),
+// dQ (fp32, one step) and dS (bf16 pairs: column c holds keys 2c and 2c+1), the
+// A operand of dQ = dS K read straight from TMEM.
+constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDK = 320, cDQ = 384, cDS = 448;
 
 struct __align__(1024) Smem {
     uint8_t k[kTile];
@@ -58,7 +60,6 @@ struct __align__(1024) Smem {
     uint64_t kv_full;
     uint64_t qdo_full[kQStages], qdo_empty[kQStages];
     uint64_t sdp_full, sdp_free, pds_full, mma2_done;  // per step
-    uint64_t dq_free[2];
     uint64_t dq_staged;     // all elementwise threads wrote their part of the dQ tile
     uint64_t dq_stage_free; // the bulk reduce has finished reading the staging buffer
     uint64_t final_bar;  // dV / dK / dQ issuer done
@@ -170,7 +171,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&S.qdo_full[s], 1);
             mbar_init(&S.qdo_empty[s], 1);
         }
-        for (int s = 0; s < 2; ++s) mbar_init(&S.dq_free[s], kWork);
         mbar_init(&S.sdp_full, 1);
         mbar_init(&S.sdp_free, kWork);
         mbar_init(&S.pds_full, kWork);
@@ -275,7 +275,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dk_mn = sdesc_sw128(smem_u32(S.k), 8192, 1024);     // K, MN-major (B of dQ)
             const uint64_t dp_mn = sdesc_sw128(smem_u32(S.pb), kTile, 1024);   // P^T, MN-major (A of dV)
             const uint64_t ds_mn = sdesc_sw128(smem_u32(S.dsb), kTile, 1024);  // dS^T, MN-major (A of dK)
-            const uint64_t ds_k = sdesc_sw128(smem_u32(S.dsb), 16, 1024);      // dS, K-major (A of dQ)
             auto wait_all = [&](uint64_t* bar, uint32_t parity) {
                 return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
             };
@@ -301,12 +300,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 for (int t = 0; ok && t < T; ++t) {
                     const int st = t % kQStages;
+                    // pds_full also means the previous dQ has been read out of TMEM
                     if (!(ok = wait_all(&S.pds_full, t & 1))) break;
-                    if (t >= 2 && !(ok = wait_all(&S.dq_free[t & 1], ((t >> 1) - 1) & 1))) break;
                     tc_fence_after();
                     const uint64_t dq_mn = sdesc_sw128(smem_u32(S.q[st]), 8192, 1024);
                     const uint64_t ddo_mn = sdesc_sw128(smem_u32(S.dout[st]), 8192, 1024);
-                    const uint32_t cq = tmem + cDQ + (t & 1) * D;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         // dV / dK: k-step kk runs over query rows 16 kk .. 16 kk + 15 of P / dS
@@ -314,10 +312,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
                         umma_ss_e(tmem + cDV, dp_mn + 128 * kk, ddo_mn + 128 * kk, idKV, acc);
                         umma_ss_e(tmem + cDK, ds_mn + 128 * kk, dq_mn + 128 * kk, idKV, acc);
-                        // dQ: k-step kk runs over keys 16 kk .. 16 kk + 15 (K-major dS: 64-key atom
-                        // kk / 4, 32 bytes per step inside it; MN-major K: 2048 bytes per step)
-                        umma_ss_e(cq, ds_k + (kk >> 2) * (kTile >> 4) + (kk & 3) * 2, dk_mn + 128 * kk, idQ,
-                                  kk > 0);
+                        // dQ: k-step kk runs over keys 16 kk .. 16 kk + 15 (dS in TMEM: 8 columns
+                        // per step; MN-major K: 2048 bytes per step)
+                        umma_ts_e(tmem + cDQ, tmem + cDS + kk * 8, dk_mn + 128 * kk, idQ, kk > 0);
                     }
                     umma_commit_e(&S.mma2_done);
                     umma_commit_e(&S.qdo_empty[st]);
@@ -426,8 +423,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                tmem_ld32(tmem + lane_base + cDQ + ((t - 1) & 1) * D + ch * 32, u);
+                tmem_ld32(tmem + lane_base + cDQ + ch * 32, u);
             }
+            // dS of this row's 64 keys into TMEM for dQ = dS K
+            tmem_st32(tmem + lane_base + cDS + ch * 32, *reinterpret_cast<uint32_t(*)[32]>(&dw[0]));
             // 64 key columns = atom ch, chunks 0..7 of 16 bytes
 #pragma unroll
             for (int cc = 0; cc < 8; ++cc) {
@@ -440,12 +439,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                              : "memory");
             }
             fence_proxy_async_smem();
+            tmem_st_wait();
+            if (t > 0) tmem_ld_wait();  // dQ of step t - 1 is out of TMEM before the next dQ GEMM
             tc_fence_before();
             mbar_arrive(&S.pds_full);
             if (t > 0) {
-                tmem_ld_wait();
-                tc_fence_before();
-                mbar_arrive(&S.dq_free[(t - 1) & 1]);
                 // the bulk reduce of step t - 2 has finished reading the stage
                 ok = t == 1 || mbar_wait(&S.dq_stage_free, (t - 2) & 1, abort);
                 if (!__all_sync(0xffffffffu, ok)) {
@@ -467,10 +465,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) {
                 tc_fence_after();
                 uint32_t u[32];
-                tmem_ld32(tmem + lane_base + cDQ + ((T - 1) & 1) * D + ch * 32, u);
+                tmem_ld32(tmem + lane_base + cDQ + ch * 32, u);
                 tmem_ld_wait();
-                tc_fence_before();
-                mbar_arrive(&S.dq_free[(T - 1) & 1]);
                 ok = __all_sync(0xffffffffu, T == 1 || mbar_wait(&S.dq_stage_free, (T - 2) & 1, abort));
                 if (ok) {
                     stage_dq(u);
