@@ -34,18 +34,18 @@ sys.path.insert(0, ROOT)
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM traffic per launch of the dominant kernel, from `ncu` captures (see
-# profiles/).  Keyed by kernel + workload; each entry records the hash of the
-# kernel source it was measured on and is reported only while that source is
-# unchanged.
+# DRAM traffic per launch of the dominant kernel (dram__bytes_read.sum +
+# dram__bytes_write.sum from an ncu capture of that kernel on the workload).
+# Keyed by kernel + workload; each entry records the hash of the kernel source
+# it was measured on and is reported only while that source is unchanged.
 NCU_TRAFFIC = {
-    # profiles/fwd_kernel_extend_varlen.md: 442.5 MB read + 258.5 MB written per launch
+    # fwd_kernel: 442.5 MB read + 258.5 MB written per launch
     "fwd_kernel/extend_varlen": {"src": "aefeee9909ec7232", "bytes": 701_026_304},
-    # profiles/bwd_main_kernel_train.md: 2.594 GB read + 1.152 GB written per launch
+    # bwd_main_kernel: 2.594 GB read + 1.152 GB written per launch
     "bwd_main_kernel/train": {"src": "42e25632af854dce", "bytes": 3_745_681_000},
-    # profiles/decode_split_kernel_decode_sink.md: decode_split_kernel, 1.944 GB + 0.011 GB
+    # decode_split_kernel: 1.944 GB + 0.011 GB
     "decode/decode_sink": {"src": "74c2b03b3cdc9cb0", "bytes": 1_954_192_080},
-    # profiles/decode_split_kernel_decode_window.md: decode_split_kernel, 1.074 GB + 0.007 GB
+    # decode_split_kernel: 1.074 GB + 0.007 GB
     "decode/decode_window": {"src": "74c2b03b3cdc9cb0", "bytes": 1_080_889_760},
 }
 
@@ -61,6 +61,15 @@ def _traffic(key, src):
     if not ent or ent["src"] != _src_hash(src):
         return None
     return ent["bytes"]
+
+
+def check_status(ext, what):
+    """The kernels report bad inputs and timed-out waits through a sticky device
+    status instead of faulting; a timed call that raised one did not do the work
+    it is credited with, so the bench fails instead of printing a number."""
+    st = ext.device_status()
+    if st != 0:
+        raise RuntimeError(f"{what}: device status {st:#x} after the timed calls")
 
 
 def load_peaks():
@@ -539,6 +548,7 @@ def main():
             r = bench_decode_append(torch, ext, dev, w, args.steps, args.warmup, flush, peaks, peak_src)
         else:
             r = bench_decode(torch, ext, dev, w, args.steps, args.warmup, flush, peaks, peak_src)
+        check_status(ext, args.only)
         if rank == 0:
             print(json.dumps({"workload": w.name, **r}))
         return
@@ -549,7 +559,9 @@ def main():
         ms, flops, roof, times = bench_extend(torch, ext, dev, p, args.steps, args.warmup, flush, peaks,
                                               peak_src, sync=lambda: rank_sync(torch, dist))
     clocks = clk.summary()
+    check_status(ext, p.name)
     e2e_ms, h2d, d2h = e2e_extend(torch, ext, dev, p, max(3, args.steps // 4), 2)
+    check_status(ext, p.name + " (host buffers)")
 
     ms_max, e2e_ms = max_over_ranks(torch, dist, [ms, e2e_ms], device=dev)
     flops_all = sum_over_ranks(torch, dist, flops, device=dev)
@@ -563,19 +575,23 @@ def main():
             r = bench_decode(torch, ext, dev, dc, args.steps, args.warmup, flush, peaks, peak_src)
             if rank == 0 and not args.no_cpu and world == 1:
                 r["cpu_baseline"] = cpu_baseline_decode(dc)
+            check_status(ext, name)
             extra[name] = r
             del dc
         tr = wl.workload("train", seed=0)
         extra["train"] = bench_train(torch, ext, dev, tr, max(3, args.steps // 2), args.warmup, flush, peaks,
                                      peak_src)
+        check_status(ext, "train")
         del tr
         pe = wl.workload("extend_paged", seed=0)
         extra["extend_paged"] = bench_extend_paged(torch, ext, dev, pe, max(3, args.steps // 2), args.warmup,
                                                    flush, peaks, peak_src)
+        check_status(ext, "extend_paged")
         del pe
         dc = wl.workload("decode_sink", seed=0)
         extra["decode_sink_append"] = bench_decode_append(torch, ext, dev, dc, args.steps, args.warmup, flush,
                                                           peaks, peak_src)
+        check_status(ext, "decode_sink_append")
         del dc
 
     line = {

@@ -101,6 +101,11 @@ enum {
  * own rows only: the value rows that its last key tile covers past its last
  * key (another request's, or beyond cu_seqlens_k[batch]) are replaced by zeros
  * in shared memory, so they may hold anything, NaN included.
+ * Input range: the online softmax exponentiates each tile against a running
+ * reference that may lag the true row maximum by up to a factor 2^64, so the
+ * un-normalised weights reach 2^64 and the fp32 accumulator of P V stays
+ * finite while max|v| * Lk < 1.8e19 (|v| < 1.7e13 at a million keys); an
+ * exact softmax would stay finite for any finite value.
  */
 int attn_sink_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v,
                   const float* sink, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
@@ -201,7 +206,9 @@ int attn_sink_decode_paged_noalloc(const attn_bf16* q, const attn_bf16* k_cache,
  *                  so request b's n_b new rows become its logical tokens
  *                  seqlens[b] - n_b .. seqlens[b] - 1
  *   page_table     (batch, max_pages) int32 device, as in attn_sink_decode_paged
- *   max_new        host upper bound of n_b (sizes the grid)
+ *   max_new        host upper bound of n_b (sizes the grid); a request with more
+ *                  new rows than max_new has its extra rows left unwritten and
+ *                  sets ATTN_SINK_DEV_SEQLEN_OOB
  *   k_cache, v_cache   (num_pages, page_size, hkv, head_dim) bf16, written in place
  * A row whose slot would fall outside the cache (page id outside
  * [0, num_pages), or more new rows than cached tokens) is skipped and sets
@@ -296,10 +303,10 @@ int attn_sink_fwd_paged(const attn_bf16* q, const attn_bf16* k_new, const attn_b
  *                of each KV head)
  *   dsink        (hq,) fp32; must be non-NULL iff sink is non-NULL; written
  *                (not accumulated)
- * Supported: head_dim 64; hq % hkv == 0.  A tile that reaches past a
- * request's last query or key row reads the next request's rows (rows past
- * total_q / total_k read as zeros) and gives them zero weight: they must be
- * finite, and then have no effect.
+ * Supported: head_dim 64; hq % hkv == 0.  A request's gradients depend on
+ * its own rows only: the rows that its last query or key tile covers past its
+ * own (another request's, or past total_q / total_k) are replaced by zeros in
+ * shared memory, so they may hold anything, NaN included.
  */
 int attn_sink_bwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, const float* sink,
                   const attn_bf16* out, const float* lse, const attn_bf16* dout,

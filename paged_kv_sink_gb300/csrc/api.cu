@@ -84,13 +84,13 @@ struct Scratch {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+}  // namespace
+
+namespace attn {
 float resolve_scale(float scale, int head_dim) {
     return scale > 0.f ? scale : 1.0f / sqrtf((float)head_dim);
 }
 
-}  // namespace
-
-namespace attn {
 // Sets the calling thread's last-error text (used by entry points defined in
 // other translation units).
 void record_error(const char* msg) { t_last_error = msg; }
@@ -104,26 +104,30 @@ const char* attn_sink_version(void) { return "attn_sink_gb300 0.1 (sm_103a)"; }
 
 }  // extern "C"
 
-namespace {
+namespace attn {
 
-int validate_decode(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_cache,
+int validate_decode(const char* who, const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_cache,
                     const int32_t* page_table, int max_pages, const int32_t* seqlens, int batch, int hq,
                     int hkv, int head_dim, int page_size, int num_pages, int win_first, attn_bf16* out) {
     if (batch < 0 || hq <= 0 || hkv <= 0 || max_pages <= 0 || page_size <= 0 || num_pages <= 0)
-        return fail(ATTN_SINK_ERR_INVALID, "decode: sizes must be positive (batch may be 0)");
-    if (win_first < 0) return fail(ATTN_SINK_ERR_INVALID, "decode: win_first must be >= 0");
+        return fail(ATTN_SINK_ERR_INVALID, "%s: sizes must be positive (batch may be 0)", who);
+    if (win_first < 0) return fail(ATTN_SINK_ERR_INVALID, "%s: win_first must be >= 0", who);
     if (head_dim != 64 && head_dim != 128)
-        return fail(ATTN_SINK_ERR_UNSUPPORTED, "decode: head_dim %d not supported (64, 128)", head_dim);
-    if (hq % hkv) return fail(ATTN_SINK_ERR_UNSUPPORTED, "decode: hq %% hkv != 0");
+        return fail(ATTN_SINK_ERR_UNSUPPORTED, "%s: head_dim %d not supported (64, 128)", who, head_dim);
+    if (hq % hkv) return fail(ATTN_SINK_ERR_UNSUPPORTED, "%s: hq %% hkv != 0", who);
     if (batch == 0) return ATTN_SINK_OK;
     if (!q || !k_cache || !v_cache || !page_table || !seqlens || !out)
-        return fail(ATTN_SINK_ERR_INVALID, "decode: NULL tensor pointer");
+        return fail(ATTN_SINK_ERR_INVALID, "%s: NULL tensor pointer", who);
     if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q) || !aligned16(out))
-        return fail(ATTN_SINK_ERR_INVALID, "decode: q, caches and out must be 16-byte aligned");
+        return fail(ATTN_SINK_ERR_INVALID, "%s: q, caches and out must be 16-byte aligned", who);
     if ((long long)num_pages * page_size >= (1LL << 31) || (long long)max_pages * page_size >= (1LL << 31))
-        return fail(ATTN_SINK_ERR_UNSUPPORTED, "decode: cache slots must fit in int32");
+        return fail(ATTN_SINK_ERR_UNSUPPORTED, "%s: cache slots must fit in int32", who);
     return ATTN_SINK_OK;
 }
+
+}  // namespace attn
+
+namespace {
 
 int run_decode(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_cache, const int32_t* page_table,
                int max_pages, const int32_t* seqlens, int batch, int hq, int hkv, int head_dim, int page_size,
@@ -148,7 +152,7 @@ int run_decode(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_
     a.win_first = win_first;
     a.win_last = win_last;
     a.group = hq / hkv;
-    a.scale = resolve_scale(scale, head_dim);
+    a.scale = attn::resolve_scale(scale, head_dim);
     attn::decode::Plan pl = attn::decode::make_plan(a);
     Scratch ws;
     cudaError_t e = ws.alloc(pl.part_o_bytes + pl.part_ml_bytes, s);
@@ -193,7 +197,7 @@ int attn_sink_decode_paged(const attn_bf16* q, const attn_bf16* k_cache, const a
                            const float* sink, int win_first, int win_last, float scale,
                            attn_bf16* out, float* lse, void* stream) {
     t_last_error.clear();
-    int rc = validate_decode(q, k_cache, v_cache, page_table, max_pages, seqlens, batch, hq, hkv, head_dim,
+    int rc = attn::validate_decode("decode", q, k_cache, v_cache, page_table, max_pages, seqlens, batch, hq, hkv, head_dim,
                              page_size, num_pages, win_first, out);
     if (rc != ATTN_SINK_OK || batch == 0) return rc;
     return run_decode(q, k_cache, v_cache, page_table, max_pages, seqlens, batch, hq, hkv, head_dim, page_size,
@@ -228,7 +232,7 @@ int attn_sink_decode_paged_append(const attn_bf16* q, const attn_bf16* k_new, co
                                   int page_size, int num_pages, const float* sink, int win_first, int win_last,
                                   float scale, attn_bf16* out, float* lse, void* stream) {
     t_last_error.clear();
-    int rc = validate_decode(q, k_cache, v_cache, page_table, max_pages, seqlens, batch, hq, hkv, head_dim,
+    int rc = attn::validate_decode("decode", q, k_cache, v_cache, page_table, max_pages, seqlens, batch, hq, hkv, head_dim,
                              page_size, num_pages, win_first, out);
     if (rc != ATTN_SINK_OK || batch == 0) return rc;
     if (!k_new || !v_new) return fail(ATTN_SINK_ERR_INVALID, "decode_append: NULL k_new / v_new");
@@ -333,7 +337,7 @@ int fwd_impl(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, long lo
     a.win_first = win_first;
     a.win_last = win_last;
     a.causal = causal ? 1 : 0;
-    a.scale = resolve_scale(scale, head_dim);
+    a.scale = attn::resolve_scale(scale, head_dim);
     a.q_rs = q_rs;
     a.k_rs = k_rs;
     a.v_rs = v_rs;
@@ -410,7 +414,7 @@ int attn_sink_fwd_host(const attn_bf16* q, const attn_bf16* k, const attn_bf16* 
     a.win_first = win_first;
     a.win_last = win_last;
     a.causal = causal ? 1 : 0;
-    a.scale = resolve_scale(scale, head_dim);
+    a.scale = attn::resolve_scale(scale, head_dim);
     if (a.total_q == 0) return ATTN_SINK_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     Scratch ws;
@@ -476,7 +480,7 @@ int attn_sink_fwd_paged(const attn_bf16* q, const attn_bf16* k_new, const attn_b
     a.win_first = win_first;
     a.win_last = win_last;
     a.causal = causal ? 1 : 0;
-    a.scale = resolve_scale(scale, head_dim);
+    a.scale = attn::resolve_scale(scale, head_dim);
     a.page_table = page_table;
     a.seqlens_k = seqlens_k;
     a.max_pages = max_pages;
@@ -533,7 +537,7 @@ int bwd_impl(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, const l
     a.win_first = win_first;
     a.win_last = win_last;
     a.causal = causal ? 1 : 0;
-    a.scale = resolve_scale(scale, head_dim);
+    a.scale = attn::resolve_scale(scale, head_dim);
     a.q_rs = rs[0];
     a.k_rs = rs[1];
     a.v_rs = rs[2];

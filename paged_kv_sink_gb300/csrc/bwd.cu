@@ -58,6 +58,8 @@ struct __align__(1024) Smem {
     uint8_t dsb[2 * kTile];  // dS (same layout)
     uint8_t dq_stage[2][kTile];  // dQ tile staging: two 32-column fp32 halves, 128-byte swizzled rows
     uint64_t kv_full;
+    uint64_t kv_ready;  // K / V rows past the request's last key zeroed (tail key tiles only)
+    uint64_t qdo_tail;  // a head's last query tile reaching past the request lands here first
     uint64_t qdo_full[kQStages], qdo_empty[kQStages];
     uint64_t sdp_full, sdp_free, pds_full, mma2_done;  // per step
     uint64_t dq_staged;     // all elementwise threads wrote their part of the dQ tile
@@ -164,9 +166,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const QRange qr = query_tiles(j0, Lq, Lk, p.causal, p.win_first, p.win_last);
     const int nqt = qr.hi - qr.lo;
     const int T = nqt * p.group;  // steps: (head g, query tile)
+    const bool kv_tail = j0 + BN > Lk;  // the key tile reaches past the request's last key
 
     if (threadIdx.x == 0) {
         mbar_init(&S.kv_full, 1);
+        mbar_init(&S.kv_ready, 1);
+        mbar_init(&S.qdo_tail, 1);
         for (int s = 0; s < kQStages; ++s) {
             mbar_init(&S.qdo_full[s], 1);
             mbar_init(&S.qdo_empty[s], 1);
@@ -197,6 +202,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp == 0) {
             // -------------------------------------------------------- producer
             // (converged warp: every lane waits, lane 0 issues the copies)
+            // Rows a tile covers past the request's own rows (another request's, or
+            // past the end of the buffers, zero-filled by TMA) enter the products
+            // with zero weight, but 0 times a NaN or an infinity would not vanish:
+            // the K / V rows past the last key and the Q / dO rows past the last
+            // query are zeroed in shared memory before the tensor core reads them
+            // (key row r and query row r are the 128 bytes at r * 128, so they
+            // form one contiguous range whatever the swizzle).
+            auto zero_rows = [&](uint8_t* tile, int r0) {
+                uint4* t4 = reinterpret_cast<uint4*>(tile);
+                for (int c = r0 * 8 + lane; c < BM * 8; c += 32) t4[c] = make_uint4(0u, 0u, 0u, 0u);
+            };
             if (lane == 0) {
                 prefetch_tmap(&tm_q);
                 prefetch_tmap(&tm_k);
@@ -206,18 +222,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(S.k, &tm_k, &S.kv_full, 0, kvh, k_start + j0);
                 tma_load_3d(S.v, &tm_v, &S.kv_full, 0, kvh, k_start + j0);
             }
-            int t = 0, g_c = 0, qt_c = 0;
-            for (; t < T; ++t) {
+            bool ok = true;
+            if (kv_tail) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&S.kv_full, 0, abort));
+                if (ok) {
+                    zero_rows(S.k, Lk - j0);
+                    zero_rows(S.v, Lk - j0);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&S.kv_ready);
+                }
+            }
+            int t = 0, g_c = 0, qt_c = 0, tails = 0;
+            bool tail_pending = false;
+            for (; ok && t < T; ++t) {
                 const int st = t % kQStages;
                 if (t >= kQStages &&
                     !__all_sync(0xffffffffu, mbar_wait(&S.qdo_empty[st], (t / kQStages - 1) & 1, abort)))
                     break;
+                const int h = kvh * p.group + g_c;
+                const int q0 = (qr.lo + qt_c) * BM;
+                const bool tail = q0 + BM > Lq;
+                uint64_t* bar = tail ? &S.qdo_tail : &S.qdo_full[st];
                 if (lane == 0) {
-                    const int h = kvh * p.group + g_c;
-                    const int q0 = (qr.lo + qt_c) * BM;
-                    mbar_expect_tx(&S.qdo_full[st], 2 * kTile);
-                    tma_load_3d(S.q[st], &tm_q, &S.qdo_full[st], 0, h, q_start + q0);
-                    tma_load_3d(S.dout[st], &tm_do, &S.qdo_full[st], 0, h, q_start + q0);
+                    mbar_expect_tx(bar, 2 * kTile);
+                    tma_load_3d(S.q[st], &tm_q, bar, 0, h, q_start + q0);
+                    tma_load_3d(S.dout[st], &tm_do, bar, 0, h, q_start + q0);
+                }
+                if (tail) {
+                    tail_pending = true;
+                    if (!__all_sync(0xffffffffu, mbar_wait(&S.qdo_tail, tails & 1, abort))) break;
+                    tail_pending = false;
+                    ++tails;
+                    zero_rows(S.q[st], Lq - q0);
+                    zero_rows(S.dout[st], Lq - q0);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&S.qdo_full[st]);
                 }
                 if (++qt_c == nqt) {
                     qt_c = 0;
@@ -226,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (lane == 0) {
                 drain_wait(&S.kv_full, 0);
+                if (tail_pending) drain_wait(&S.qdo_tail, tails & 1);
                 for (int st = 0; st < kQStages; ++st) {
                     const int n = t > st ? (t - st + kQStages - 1) / kQStages : 0;  // loads issued into stage st
                     if (n > 0) drain_wait(&S.qdo_full[st], (n - 1) & 1);
@@ -278,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto wait_all = [&](uint64_t* bar, uint32_t parity) {
                 return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
             };
-            bool ok = wait_all(&S.kv_full, 0);
+            bool ok = wait_all(kv_tail ? &S.kv_ready : &S.kv_full, 0);
             if (warp == 1) {
                 for (int t = 0; ok && t < T; ++t) {
                     const int st = t % kQStages;
@@ -343,7 +385,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // fp32 accumulator with TMA bulk reduce-adds.  dS carries the softmax scale,
         // so the values go out as they are.
         uint32_t* const stage_row = reinterpret_cast<uint32_t*>(S.dq_stage[ch] + i * 128);
-        auto stage_dq = [&](const uint32_t (&u)[32]) {
+        // Query rows past the request's end (another request's rows) are staged as
+        // zeros: their dS is zero, but times a non-finite key it would not be.
+        auto stage_dq = [&](uint32_t (&u)[32], int q0_row) {
+            if (q0_row + i >= Lq) {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) u[c] = 0u;
+            }
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(smem_u32(stage_row) + (((c ^ (i & 7))) << 4)),
@@ -366,6 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // step t = g_c * nqt + qt_c (head g_c of the group, query tile qt_c)
         int g_c = 0, qt_c = 0;
+        int q0_prev = 0;  // first query row of the previous step's tile
         float lse_cur, d_cur;
         load_row(0, 0, lse_cur, d_cur);
         for (int t = 0; t < T; ++t) {
@@ -450,10 +499,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                stage_dq(u);
+                stage_dq(u, q0_prev);
                 fence_proxy_async_smem();
                 mbar_arrive(&S.dq_staged);
             }
+            q0_prev = q0;
             lse_cur = lse_nxt;
             d_cur = d_nxt;
             g_c = g_n;
@@ -469,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_wait();
                 ok = __all_sync(0xffffffffu, T == 1 || mbar_wait(&S.dq_stage_free, (T - 2) & 1, abort));
                 if (ok) {
-                    stage_dq(u);
+                    stage_dq(u, q0_prev);
                     fence_proxy_async_smem();
                     mbar_arrive(&S.dq_staged);
                 }
@@ -525,8 +575,12 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
                                                              const __nv_bfloat16* __restrict__ dout,
                                                              const float* __restrict__ lse,
                                                              const float* __restrict__ sink, float* __restrict__ dvec,
-                                                             float* __restrict__ dsink, int total_q, int hq) {
+                                                             float* __restrict__ dsink, int total_q, int hq,
+                                                             const int32_t* __restrict__ cu_q, int batch) {
     const int h = blockIdx.y;
+    // Rows past the last request (cu_q[batch] <= row < total_q) belong to no
+    // request: D = 0 and no sink term, whatever the buffers hold there.
+    const int rows = min(total_q, max(0, cu_q[batch]));
     const int tid = threadIdx.x;
     const int sub = tid & 7;
     const float sg = sink ? sink[h] : -INFINITY;
@@ -534,7 +588,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
     for (int rr = 0; rr < 2; ++rr) {
         const int row = blockIdx.x * 64 + rr * 32 + (tid >> 3);
         float d = 0.f;
-        if (row < total_q) {
+        if (row < rows) {
             const size_t base = ((size_t)row * hq + h) * D + sub * 8;
             const uint4 o = *reinterpret_cast<const uint4*>(out + base);
             const uint4 g = *reinterpret_cast<const uint4*>(dout + base);
@@ -547,7 +601,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
         d += __shfl_xor_sync(0xffffffffu, d, 4);
         if (row < total_q && sub == 0) {
             dvec[(size_t)h * total_q + row] = d;
-            if (sink) {
+            if (sink && row < rows) {
                 const float l = lse[(size_t)h * total_q + row];
                 // probability mass on the sink, e^{sink - LSE}
                 float ps;
@@ -677,7 +731,7 @@ cudaError_t launch(const Args& a, void* workspace, size_t ws_bytes, cudaStream_t
         dim3 g1((a.total_q + 63) / 64, a.hq);
         bwd_preprocess_kernel<<<g1, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(a.out),
                                                  reinterpret_cast<const __nv_bfloat16*>(a.dout), a.lse, a.sink,
-                                                 dvec, a.dsink, a.total_q, a.hq);
+                                                 dvec, a.dsink, a.total_q, a.hq, a.cu_q, a.batch);
         if ((e = cudaGetLastError()) != cudaSuccess) {
             *what = "preprocess launch";
             return e;

@@ -112,6 +112,10 @@ __device__ __forceinline__ Ranges request_ranges(const SplitParams& p, int b, bo
 template <int D, int NT, int NSTAGE>
 __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
+    // Per staged token row: 1 if it holds a visible token read through a valid
+    // page, 0 if it was zero-filled (past the split, or an out-of-range page id);
+    // invalid rows get a score of -inf, so they take no weight in the softmax.
+    __shared__ uint8_t row_ok[NSTAGE][kChunk];
     constexpr int kStageBytes = 2 * kChunk * D * 2;
     constexpr int kSegs = D / 8;                        // 16-byte segments per row
 
@@ -123,9 +127,10 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitParam
 
     const Ranges r = request_ranges(p, b, tid == 0 && split == 0 && blockIdx.y == 0);
     const int nvis = visible_count(r);
-    const int v0 = split * p.split_tokens;
-    if (v0 >= nvis) return;
-    const int v1 = min(nvis, v0 + p.split_tokens);
+    const long long v0l = (long long)split * p.split_tokens;
+    if (v0l >= nvis) return;
+    const int v0 = (int)v0l;
+    const int v1 = (int)min((long long)nvis, v0l + p.split_tokens);
     const int nchunks = (v1 - v0 + kChunk - 1) / kChunk;
 
     const int h_base = kvh * p.group + hb * 8 * NT;
@@ -160,6 +165,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitParam
         int slot = -1;
         if (lane < 16) {
             const int row = ((lane / kRowsPerInst) * 4 + warp) * kRowsPerInst + (lane % kRowsPerInst);
+            row_ok[stage][row] = 0;
             const int v = v0 + c * kChunk + row;
             if (v < v1) {
                 const int t = visible_token(r, v);
@@ -172,10 +178,12 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitParam
                     in_pg = t - pg * p.page_size;
                 }
                 const int page = p.page_table[(size_t)b * p.max_pages + pg];
-                if ((unsigned)page < (unsigned)p.num_pages)
+                if ((unsigned)page < (unsigned)p.num_pages) {
                     slot = page * p.page_size + in_pg;
-                else
+                    row_ok[stage][row] = 1;
+                } else {
                     raise_status(ATTN_SINK_DEV_PAGE_OOB);
+                }
             }
         }
 #pragma unroll
@@ -235,8 +243,8 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitParam
             for (int nt = 0; nt < NT; ++nt) mma_16816(sacc[nt], a, qf[nt][kk]);
         }
 
-        const int tok = v0 + c * kChunk + warp * 16 + (lane >> 2);
-        const bool ok0 = tok < v1, ok1 = tok + 8 < v1;
+        const int crow = warp * 16 + (lane >> 2);
+        const bool ok0 = row_ok[c % NSTAGE][crow] != 0, ok1 = row_ok[c % NSTAGE][crow + 8] != 0;
         uint32_t pf[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
@@ -336,7 +344,7 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const SplitParams p, 
     const int h = blockIdx.x, b = blockIdx.y, dd = threadIdx.x;
     const Ranges r = request_ranges(p, b, false);
     const int nvis = visible_count(r);
-    const int nsplit = (nvis + p.split_tokens - 1) / p.split_tokens;
+    const int nsplit = (int)(((long long)nvis + p.split_tokens - 1) / p.split_tokens);
     const size_t base = ((size_t)b * p.hq + h) * p.max_splits;
     const float sg = sink ? sink[h] * ATTN_LOG2E : -INFINITY;
     float M = sg;
@@ -435,6 +443,7 @@ Plan make_plan(const Args& a) {
     const int split = (int)sp;
     pl.split_tokens = split;
     pl.max_splits = (int)((nvis_max + split - 1) / split);
+    pl.nvis_max = nvis_max;
     pl.part_o_bytes = (size_t)a.batch * a.hq * pl.max_splits * a.head_dim * sizeof(float);
     pl.part_ml_bytes = (size_t)a.batch * a.hq * pl.max_splits * sizeof(float2);
     return pl;

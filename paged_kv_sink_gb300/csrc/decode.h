@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "attn_sink.h"
+
 namespace attn {
 namespace decode {
 
@@ -44,6 +46,7 @@ struct Plan {
     int hblocks;       // CTAs per KV head along the query-head axis
     int split_tokens;  // visible tokens per split
     int max_splits;    // splits of the longest possible request
+    long long nvis_max;  // visible tokens of the longest possible request
     size_t part_o_bytes, part_ml_bytes;
 };
 
@@ -59,5 +62,13 @@ int status_exchange(cudaStream_t s, int* host_bits);
 }  // namespace decode
 
 void record_error(const char* msg);
+
+// Argument checks of the paged decode entry points (api.cu); `who` prefixes the
+// error text.  Returns an ATTN_SINK_* status and records the error text.
+int validate_decode(const char* who, const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_cache,
+                    const int32_t* page_table, int max_pages, const int32_t* seqlens, int batch, int hq,
+                    int hkv, int head_dim, int page_size, int num_pages, int win_first, attn_bf16* out);
+// The softmax scale: `scale` if positive, else 1/sqrt(head_dim).
+float resolve_scale(float scale, int head_dim);
 
 }  // namespace attn

@@ -12,6 +12,7 @@
 #include <math.h>
 #include <stdio.h>
 
+#include <algorithm>
 #include <mutex>
 #include <string>
 
@@ -64,20 +65,9 @@ int attn_sink_decode_paged_noalloc(const attn_bf16* q, const attn_bf16* k_cache,
         attn::record_error(msg);
         return code;
     };
-    if (batch < 0 || hq <= 0 || hkv <= 0 || max_pages <= 0 || page_size <= 0 || num_pages <= 0 ||
-        win_first < 0)
-        return fail(ATTN_SINK_ERR_INVALID, "decode_noalloc: sizes must be positive (batch may be 0)");
-    if (head_dim != 64 && head_dim != 128)
-        return fail(ATTN_SINK_ERR_UNSUPPORTED, "decode_noalloc: head_dim must be 64 or 128");
-    if (hq % hkv) return fail(ATTN_SINK_ERR_UNSUPPORTED, "decode_noalloc: hq is not a multiple of hkv");
-    if (batch == 0) return ATTN_SINK_OK;
-    if (!q || !k_cache || !v_cache || !page_table || !seqlens || !out)
-        return fail(ATTN_SINK_ERR_INVALID, "decode_noalloc: NULL tensor pointer");
-    auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-    if (!a16(q) || !a16(k_cache) || !a16(v_cache) || !a16(out))
-        return fail(ATTN_SINK_ERR_INVALID, "decode_noalloc: q, caches and out must be 16-byte aligned");
-    if ((long long)num_pages * page_size >= (1LL << 31) || (long long)max_pages * page_size >= (1LL << 31))
-        return fail(ATTN_SINK_ERR_UNSUPPORTED, "decode_noalloc: cache slots must fit in int32");
+    int rc = attn::validate_decode("decode_noalloc", q, k_cache, v_cache, page_table, max_pages, seqlens, batch, hq,
+                                   hkv, head_dim, page_size, num_pages, win_first, out);
+    if (rc != ATTN_SINK_OK || batch == 0) return rc;
 
     attn::decode::Args a;
     a.q = q;
@@ -98,7 +88,7 @@ int attn_sink_decode_paged_noalloc(const attn_bf16* q, const attn_bf16* k_cache,
     a.win_first = win_first;
     a.win_last = win_last;
     a.group = hq / hkv;
-    a.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)head_dim);
+    a.scale = attn::resolve_scale(scale, head_dim);
 
     // Same work split as the allocating entry point; when its partials do not
     // fit, use fewer, longer splits (the result differs only by rounding).
@@ -107,10 +97,14 @@ int attn_sink_decode_paged_noalloc(const attn_bf16* q, const attn_bf16* k_cache,
         const size_t o = (p.part_o_bytes + 255) & ~size_t(255);
         return o + p.part_ml_bytes;
     };
+    // Longer splits: double the split length, but never past the longest request
+    // (rounded to whole 64-token chunks, and kept below 2^31 tokens).
+    const long long cap = std::min((pl.nvis_max + 63) / 64 * 64, (1LL << 31) - 64);
     while (need(pl) > kScratchBytes && pl.max_splits > 1) {
-        const long long nvis_max = (long long)pl.max_splits * pl.split_tokens;
-        pl.split_tokens *= 2;
-        pl.max_splits = (int)((nvis_max + pl.split_tokens - 1) / pl.split_tokens);
+        const long long st = std::min(2LL * pl.split_tokens, cap);
+        if (st == pl.split_tokens) break;  // already one split per request (or at the cap)
+        pl.split_tokens = (int)st;
+        pl.max_splits = (int)((pl.nvis_max + st - 1) / st);
         pl.part_o_bytes = (size_t)batch * hq * pl.max_splits * head_dim * sizeof(float);
         pl.part_ml_bytes = (size_t)batch * hq * pl.max_splits * sizeof(float2);
     }

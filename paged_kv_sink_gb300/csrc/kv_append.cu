@@ -10,7 +10,8 @@
 //
 // One block per (request, 8 new rows); each row (Hkv * d bf16) is moved with
 // 16-byte loads and stores.  A slot outside the cache or a request with fewer
-// tokens than new rows raises a device status bit and skips the row.
+// tokens than new rows raises a device status bit and skips the row, and so
+// does a request with more new rows than the grid covers (max_new).
 #include "common.cuh"
 #include "kv_append.h"
 
@@ -32,6 +33,10 @@ __global__ void __launch_bounds__(kThreads) kv_append_kernel(const uint4* __rest
     const int n = cu_new ? cu_new[b + 1] - n0 : 1;
     const int L = seqlens[b];
     const int r_begin = blockIdx.x * kRowsPerBlock;
+    // The grid covers max_new rows per request; a request with more new rows
+    // than that would leave rows unwritten: flag it.
+    if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0 && n > (int)gridDim.x * kRowsPerBlock)
+        raise_status(ATTN_SINK_DEV_SEQLEN_OOB);
     for (int idx = threadIdx.x; idx < kRowsPerBlock * vec_per_row; idx += kThreads) {
         const int r = r_begin + idx / vec_per_row;
         const int c = idx % vec_per_row;

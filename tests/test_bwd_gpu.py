@@ -53,6 +53,9 @@ CASES = {
     "sliding_only": ([300], [500], 2, 1, "normal", 0, 64, True),
     "more_q_than_k": ([300, 10], [100, 0], 4, 2, "normal", 0, 0, True),
     "group8": ([512], [1024], 16, 2, (-2.0, 4.0), 0, 0, True),
+    # the sglang window (first 1024 + last 7168) past 8192 keys: the key tiles in the
+    # gap between the windows see no query row, a first window wider than a tile
+    "window_1024_7168": ([384], [9000], 2, 1, (-2.0, 4.0), 1024, 7168, True),
 }
 
 

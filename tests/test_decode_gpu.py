@@ -167,6 +167,27 @@ def test_bad_page_ids_and_lengths_raise_device_status(ext):
     assert ext.device_status() & 2
 
 
+def test_bad_page_rows_take_no_weight(ext):
+    """Rows read through an out-of-range page id are skipped (status bit) and
+    left out of the softmax: the result equals the decode over the request's
+    other tokens (built as a shorter request whose page table skips that page)."""
+    dc = wl.make_decode(seqlens=[40, 40], hq=4, hkv=1, d=64, page_size=16, sink=("uniform", -2.0, 4.0), seed=7)
+    pt = dc.page_table.clone()
+    pt[1, 1] = dc.num_pages + 100  # request 1, tokens 16..31
+    t = _dev(dc)
+    ext.device_status()
+    out, lse = ext.attn_sink_decode_paged(t["q"], t["k_cache"], t["v_cache"], pt.cuda(), t["seqlens"], t["sink"])
+    torch.cuda.synchronize()
+    assert ext.device_status() & ext._lib.DEV_PAGE_OOB
+    # request 1 without tokens 16..31: tokens 0..15 (page pt[1,0]) then 32..39 (slots 0..7 of page pt[1,2])
+    pt2 = dc.page_table.clone()
+    pt2[1, 1] = dc.page_table[1, 2]
+    sl2 = torch.tensor([40, 24], dtype=torch.int32)
+    O, LSE = orc.attn_decode_paged(dc.q, dc.k_cache, dc.v_cache, pt2, sl2, dc.page_size, dc.sink)
+    assert_out_close(out.cpu(), O)
+    assert_lse_close(lse.cpu(), LSE)
+
+
 @pytest.mark.parametrize("name", ["decode_sink", "decode_window"])
 def test_full_size_workloads_sampled(ext, name):
     """The full-size decode workloads, in the launch configuration the bench

@@ -251,6 +251,25 @@ def test_kv_append_bad_rows_are_skipped_and_flagged(ext):
             assert torch.equal(flat_got[sl], flat_old[sl])
 
 
+def test_kv_append_rows_past_max_new_are_flagged(ext):
+    """max_new sizes the grid: a request with more new rows than the grid covers
+    leaves its extra rows unwritten and raises the sequence-length status bit."""
+    pe = wl.make_paged_extend(seqlens_q=[10, 1], seqlens_k=[30, 5], hq=2, hkv=2, d=64, page_size=16, seed=4)
+    dev = "cuda"
+    kc, vc = pe.k_cache.to(dev), pe.v_cache.to(dev)
+    ext.device_status()
+    ext.attn_sink_kv_append(pe.k_new.to(dev), pe.v_new.to(dev), kc, vc, pe.page_table.to(dev),
+                            pe.seqlens_k.to(dev), cu_new=pe.cu_seqlens_q.to(dev), max_new=2)
+    torch.cuda.synchronize()
+    assert ext.device_status() & ext._lib.DEV_SEQLEN_OOB
+    # the grid covers 8 rows per request: request 0's rows 0..7 land, rows 8 and 9 do not
+    pt0 = pe.page_table.numpy()
+    flat_got, flat_old = kc.cpu().reshape(-1, 2, 64), pe.k_cache.reshape(-1, 2, 64)
+    for r in range(10):
+        sl = orc.paged_slot(pt0, 0, 20 + r, 16)
+        assert torch.equal(flat_got[sl], pe.k_new[r] if r < 8 else flat_old[sl])
+
+
 def test_fwd_paged_bad_page_is_flagged(ext):
     pe = wl.make_paged_extend(seqlens_q=[64], seqlens_k=[200], hq=2, hkv=1, d=64, page_size=16, seed=2)
     pt = pe.page_table.clone()

@@ -1,7 +1,10 @@
 """Rows that a request's last key tile covers past its own keys must not reach its
 output: with NaN in every cache slot no request owns, and NaN in a neighbouring
 request's rows and past the end of the K/V buffers, the forward's outputs equal
-those of the clean inputs bit for bit."""
+those of the clean inputs bit for bit.  The backward likewise: NaN in a
+neighbouring request and past the end of q, dout, k and v leaves the other
+requests' gradients as they are (dK and dV bit for bit; dQ and dsink are sums
+of fp32 atomic adds whose order is not fixed)."""
 import pytest
 import torch
 
@@ -79,3 +82,63 @@ def test_fwd_neighbour_and_trailing_rows_do_not_leak(ext):
         assert not results[0][0][lo:hi].isnan().any()
         assert torch.equal(results[0][0][lo:hi], results[1][0][lo:hi])
         assert torch.equal(results[0][1][:, lo:hi], results[1][1][:, lo:hi])
+
+
+def _fwd_bwd(ext, q, k, v, dout, p, dev="cuda"):
+    sink = p.sink.to(dev)
+    cq, ck = p.cu_seqlens_q.to(dev), p.cu_seqlens_k.to(dev)
+    q, k, v, dout = q.to(dev), k.to(dev), v.to(dev), dout.to(dev)
+    out, lse = ext.attn_sink_fwd(q, k, v, sink, cq, ck, p.max_seqlen_q, p.max_seqlen_k)
+    dq, dk, dv, ds = ext.attn_sink_bwd(q, k, v, sink, out, lse, dout, cq, ck, p.max_seqlen_q, p.max_seqlen_k)
+    torch.cuda.synchronize()
+    assert ext.device_status() == 0
+    return dq.cpu(), dk.cpu(), dv.cpu(), ds.cpu()
+
+
+def _rel(a, b):
+    a, b = a.double(), b.double()
+    return float((a - b).norm() / max(float(b.norm()), 1e-30))
+
+
+def test_bwd_trailing_rows_do_not_leak(ext):
+    """64 NaN rows past the end of q, dout, k and v (the last request's tail tiles
+    read them): every gradient, dsink included, is unchanged."""
+    p = wl.make_prefill(seqlens_q=[100, 77, 129], seqlens_k=[300, 200, 129], hq=8, hkv=2, d=64, sink="normal",
+                        with_dout=True, seed=29)
+    res = []
+    for poison in (False, True):
+        q, k, v, dout = p.q.clone(), p.k.clone(), p.v.clone(), p.dout.clone()
+        if poison:
+            def pad(x):
+                return torch.cat([x, torch.full((64,) + tuple(x.shape[1:]), float("nan"), dtype=x.dtype)])
+            q, k, v, dout = pad(q), pad(k), pad(v), pad(dout)
+        dq, dk, dv, ds = _fwd_bwd(ext, q, k, v, dout, p)
+        res.append((dq[:p.q.shape[0]], dk[:p.k.shape[0]], dv[:p.k.shape[0]], ds))
+    (dq0, dk0, dv0, ds0), (dq1, dk1, dv1, ds1) = res
+    for x in (dq1, dk1, dv1, ds1):
+        assert not x.isnan().any()
+    assert torch.equal(dk0, dk1) and torch.equal(dv0, dv1)
+    assert _rel(dq1, dq0) <= 1e-5 and _rel(ds1, ds0) <= 1e-5
+
+
+def test_bwd_neighbour_rows_do_not_leak(ext):
+    """Request 1 holds NaN in every row of q, dout, k and v: the gradients of
+    requests 0 and 2 (whose tail tiles cover request 1's rows and the buffers'
+    end) stay finite and unchanged."""
+    p = wl.make_prefill(seqlens_q=[100, 77, 129], seqlens_k=[300, 200, 129], hq=8, hkv=2, d=64, sink="normal",
+                        with_dout=True, seed=31)
+    cq, ck = p.cu_seqlens_q.tolist(), p.cu_seqlens_k.tolist()
+    res = []
+    for poison in (False, True):
+        q, k, v, dout = p.q.clone(), p.k.clone(), p.v.clone(), p.dout.clone()
+        if poison:
+            q[cq[1]:cq[2]] = float("nan")
+            dout[cq[1]:cq[2]] = float("nan")
+            k[ck[1]:ck[2]] = float("nan")
+            v[ck[1]:ck[2]] = float("nan")
+        res.append(_fwd_bwd(ext, q, k, v, dout, p))
+    (dq0, dk0, dv0, _), (dq1, dk1, dv1, _) = res
+    for (ql, qh), (kl, kh) in (((cq[0], cq[1]), (ck[0], ck[1])), ((cq[2], cq[3]), (ck[2], ck[3]))):
+        assert not dq1[ql:qh].isnan().any() and not dk1[kl:kh].isnan().any() and not dv1[kl:kh].isnan().any()
+        assert torch.equal(dk0[kl:kh], dk1[kl:kh]) and torch.equal(dv0[kl:kh], dv1[kl:kh])
+        assert _rel(dq1[ql:qh], dq0[ql:qh]) <= 1e-5
