@@ -279,13 +279,15 @@ static int validate_varlen(const char* who, const void* q, const void* k, const 
                            const int32_t* cu_q, const int32_t* cu_k, int batch, int total_q,
                            int total_k, int hq, int hkv,
                            int head_dim, int max_seqlen_q, int max_seqlen_k, int win_first,
-                           int win_last, int causal) {
+                           int win_last, int causal, bool allow_d128) {
     if (batch < 0 || total_q < 0 || total_k < 0 || hq <= 0 || hkv <= 0 || max_seqlen_q < 0 ||
         max_seqlen_k < 0 || win_first < 0)
         return fail(ATTN_SINK_ERR_INVALID, "%s: sizes must be non-negative (heads positive)", who);
     if (win_last > 0 && !causal)
         return fail(ATTN_SINK_ERR_INVALID, "%s: first/last-window selection needs causal attention", who);
-    if (head_dim != 64) return fail(ATTN_SINK_ERR_UNSUPPORTED, "%s: head_dim %d not supported (64)", who, head_dim);
+    if (head_dim != 64 && !(allow_d128 && head_dim == 128))
+        return fail(ATTN_SINK_ERR_UNSUPPORTED, "%s: head_dim %d not supported (%s)", who, head_dim,
+                    allow_d128 ? "64, 128" : "64");
     if (hq % hkv) return fail(ATTN_SINK_ERR_UNSUPPORTED, "%s: hq %% hkv != 0", who);
     if (batch == 0) return ATTN_SINK_OK;
     if (!q || !k || !v || !cu_q || !cu_k) return fail(ATTN_SINK_ERR_INVALID, "%s: NULL tensor pointer", who);
@@ -300,11 +302,11 @@ namespace {
 
 // A row stride (elements) is 0 (contiguous) or covers the row's heads and keeps
 // every row 16-byte aligned.
-int check_stride(const char* who, const char* name, long long rs, int heads) {
+int check_stride(const char* who, const char* name, long long rs, int heads, int head_dim) {
     if (rs == 0) return ATTN_SINK_OK;
-    if (rs < (long long)heads * 64 || rs % 8)
-        return fail(ATTN_SINK_ERR_INVALID, "%s: %s row stride %lld must be 0 or >= heads*64 and a multiple of 8", who,
-                    name, rs);
+    if (rs < (long long)heads * head_dim || rs % 8)
+        return fail(ATTN_SINK_ERR_INVALID,
+                    "%s: %s row stride %lld must be 0 or >= heads*head_dim and a multiple of 8", who, name, rs);
     return ATTN_SINK_OK;
 }
 
@@ -313,7 +315,7 @@ int fwd_impl(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, long lo
              int total_q, int total_k, int hq, int hkv, int head_dim, int max_seqlen_q, int max_seqlen_k,
              int win_first, int win_last, int causal, float scale, attn_bf16* out, float* lse, void* stream) {
     int rc = validate_varlen("fwd", q, k, v, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, hq, hkv, head_dim,
-                             max_seqlen_q, max_seqlen_k, win_first, win_last, causal);
+                             max_seqlen_q, max_seqlen_k, win_first, win_last, causal, true);
     if (rc != ATTN_SINK_OK || batch == 0 || max_seqlen_q == 0 || total_q == 0) return rc;
     if (!out) return fail(ATTN_SINK_ERR_INVALID, "fwd: NULL out");
     if (!aligned16(out)) return fail(ATTN_SINK_ERR_INVALID, "fwd: out must be 16-byte aligned");
@@ -369,9 +371,9 @@ int attn_sink_fwd_strided(const attn_bf16* q, const attn_bf16* k, const attn_bf1
                           void* stream) {
     t_last_error.clear();
     int rc;
-    if ((rc = check_stride("fwd_strided", "q", q_row_stride, hq)) != ATTN_SINK_OK ||
-        (rc = check_stride("fwd_strided", "k", k_row_stride, hkv)) != ATTN_SINK_OK ||
-        (rc = check_stride("fwd_strided", "v", v_row_stride, hkv)) != ATTN_SINK_OK)
+    if ((rc = check_stride("fwd_strided", "q", q_row_stride, hq, head_dim)) != ATTN_SINK_OK ||
+        (rc = check_stride("fwd_strided", "k", k_row_stride, hkv, head_dim)) != ATTN_SINK_OK ||
+        (rc = check_stride("fwd_strided", "v", v_row_stride, hkv, head_dim)) != ATTN_SINK_OK)
         return rc;
     return fwd_impl(q, k, v, q_row_stride, k_row_stride, v_row_stride, sink, cu_seqlens_q, cu_seqlens_k, batch,
                     total_q, total_k, hq, hkv, head_dim, max_seqlen_q, max_seqlen_k, win_first, win_last, causal,
@@ -387,7 +389,8 @@ int attn_sink_fwd_host(const attn_bf16* q, const attn_bf16* k, const attn_bf16* 
         return fail(ATTN_SINK_ERR_INVALID, "fwd_host: sizes must be non-negative (heads positive)");
     if (win_last > 0 && !causal)
         return fail(ATTN_SINK_ERR_INVALID, "fwd_host: first/last-window selection needs causal attention");
-    if (head_dim != 64) return fail(ATTN_SINK_ERR_UNSUPPORTED, "fwd_host: head_dim %d not supported (64)", head_dim);
+    if (head_dim != 64 && head_dim != 128)
+        return fail(ATTN_SINK_ERR_UNSUPPORTED, "fwd_host: head_dim %d not supported (64, 128)", head_dim);
     if (hq % hkv) return fail(ATTN_SINK_ERR_UNSUPPORTED, "fwd_host: hq %% hkv != 0");
     if (batch == 0) return ATTN_SINK_OK;
     if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_k || !out)
@@ -411,6 +414,7 @@ int attn_sink_fwd_host(const attn_bf16* q, const attn_bf16* k, const attn_bf16* 
     a.total_k = cu_seqlens_k[batch];
     a.hq = hq;
     a.hkv = hkv;
+    a.head_dim = head_dim;
     a.win_first = win_first;
     a.win_last = win_last;
     a.causal = causal ? 1 : 0;
@@ -438,8 +442,8 @@ int attn_sink_fwd_paged(const attn_bf16* q, const attn_bf16* k_new, const attn_b
         return fail(ATTN_SINK_ERR_INVALID, "fwd_paged: sizes must be non-negative (heads, pages positive)");
     if (win_last > 0 && !causal)
         return fail(ATTN_SINK_ERR_INVALID, "fwd_paged: first/last-window selection needs causal attention");
-    if (head_dim != 64)
-        return fail(ATTN_SINK_ERR_UNSUPPORTED, "fwd_paged: head_dim %d not supported (64)", head_dim);
+    if (head_dim != 64 && head_dim != 128)
+        return fail(ATTN_SINK_ERR_UNSUPPORTED, "fwd_paged: head_dim %d not supported (64, 128)", head_dim);
     if (hq % hkv) return fail(ATTN_SINK_ERR_UNSUPPORTED, "fwd_paged: hq %% hkv != 0");
     if (page_size < 8 || (page_size & (page_size - 1)))
         return fail(ATTN_SINK_ERR_UNSUPPORTED, "fwd_paged: page_size %d not supported (a power of two >= 8)",
@@ -502,7 +506,7 @@ int bwd_impl(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, const l
              int max_seqlen_q, int max_seqlen_k, int win_first, int win_last, int causal, float scale,
              attn_bf16* dq, attn_bf16* dk, attn_bf16* dv, float* dsink, void* stream) {
     int rc = validate_varlen("bwd", q, k, v, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, hq, hkv, head_dim,
-                             max_seqlen_q, max_seqlen_k, win_first, win_last, causal);
+                             max_seqlen_q, max_seqlen_k, win_first, win_last, causal, false);
     if (rc != ATTN_SINK_OK) return rc;
     if ((sink == nullptr) != (dsink == nullptr))
         return fail(ATTN_SINK_ERR_INVALID, "bwd: dsink must be given exactly when sink is");
@@ -585,7 +589,7 @@ int attn_sink_bwd_strided(const attn_bf16* q, const attn_bf16* k, const attn_bf1
                              dv_row_stride};
     const char* names[6] = {"q", "k", "v", "dq", "dk", "dv"};
     for (int i = 0; i < 6; ++i)
-        if ((rc = check_stride("bwd_strided", names[i], rs[i], (i % 3) == 0 ? hq : hkv)) != ATTN_SINK_OK) return rc;
+        if ((rc = check_stride("bwd_strided", names[i], rs[i], (i % 3) == 0 ? hq : hkv, head_dim)) != ATTN_SINK_OK) return rc;
     return bwd_impl(q, k, v, rs, sink, out, lse, dout, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, hq,
                     hkv, head_dim, max_seqlen_q, max_seqlen_k, win_first, win_last, causal, scale, dq, dk, dv,
                     dsink, stream);

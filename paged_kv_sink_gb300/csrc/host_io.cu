@@ -77,7 +77,7 @@ cudaError_t run(const Args& a, void* dev_buf, cudaStream_t caller, std::string* 
         *what = "streams";
         return e;
     }
-    const size_t q_row = (size_t)a.hq * 64 * 2, kv_row = (size_t)a.hkv * 64 * 2;
+    const size_t q_row = (size_t)a.hq * a.head_dim * 2, kv_row = (size_t)a.hkv * a.head_dim * 2;
     char* p = static_cast<char*>(dev_buf);
     auto carve = [&](size_t bytes) {
         char* r = p;
@@ -156,7 +156,7 @@ cudaError_t run(const Args& a, void* dev_buf, cudaStream_t caller, std::string* 
         f.total_k = k1;
         f.hq = a.hq;
         f.hkv = a.hkv;
-        f.head_dim = 64;
+        f.head_dim = a.head_dim;
         f.max_seqlen_q = Lq;
         f.max_seqlen_k = Lk;
         f.win_first = a.win_first;
@@ -187,7 +187,7 @@ cudaError_t run(const Args& a, void* dev_buf, cudaStream_t caller, std::string* 
 
 size_t scratch_bytes(const Args& a) {
     auto r = [](size_t b) { return (b + 255) & ~size_t(255); };
-    const size_t q_row = (size_t)a.hq * 64 * 2, kv_row = (size_t)a.hkv * 64 * 2;
+    const size_t q_row = (size_t)a.hq * a.head_dim * 2, kv_row = (size_t)a.hkv * a.head_dim * 2;
     return 2 * r((size_t)a.total_q * q_row) + 2 * r((size_t)a.total_k * kv_row) + r((size_t)a.hq * a.total_q * 4) +
            r((size_t)a.hq * 4) + 2 * r((size_t)(a.batch + 1) * 4);
 }

@@ -20,7 +20,7 @@ struct Args {
     const int32_t* cu_k;
     void* out;
     float* lse;
-    int batch, total_q, total_k, hq, hkv, win_first, win_last, causal;
+    int batch, total_q, total_k, hq, hkv, head_dim, win_first, win_last, causal;
     float scale;
 };
 

@@ -42,7 +42,6 @@ using namespace sm103;
 
 constexpr int BM = 128;
 constexpr int BN = 128;
-constexpr int D = 64;
 constexpr int KSTAGE = 3;
 constexpr int VSTAGE = 3;
 constexpr int kThreads = 256;
@@ -51,19 +50,31 @@ constexpr int kThreads = 256;
 // 128*40 + 128*216 = 32768 = 256 threads * 128.
 constexpr int kRegsCtrl = 40;
 constexpr int kRegsSoftmax = 216;
-constexpr uint32_t kTile = 128 * 128;  // 128 rows x 128 bytes
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t cS = 0, cO = 128, cP = 192;  // TMEM columns
+constexpr uint32_t kAtom = 128 * 128;  // one 128-byte-swizzled atom column: 128 rows x 64 bf16
+// Head-dim dependent sizes.  An operand tile of 128 rows is D / 64 atoms, atom a
+// holding elements 64a .. 64a + 63 of every row at byte offset a * kAtom.
+// TMEM: S at column 0 (128 fp32), O at 128 (D fp32), P at 128 + D (64 columns
+// of bf16 pairs); d 64 fits two CTAs per SM (256 columns each), d 128 takes
+// one CTA and all 512 columns.
+template <int D>
+struct Cfg {
+    static constexpr int kAtoms = D / 64;
+    static constexpr uint32_t kTile = kAtom * kAtoms;
+    static constexpr uint32_t kTmemCols = D == 64 ? 256 : 512;
+    static constexpr uint32_t cS = 0, cO = 128, cP = 128 + D;
+    static constexpr bool kTwoPerSm = D == 64;
+};
 // The running reference max only moves when a row's max exceeds it by more
 // than 2^64 (log2 units below); every P value stays below 2^64 and every sum
 // far below fp32's range, so the stale reference costs no accuracy.
 constexpr float kRescaleThreshold = 64.0f;
 constexpr float kFastSumLimit = 1.8446744e19f;  // 2^64
 
+template <int D>
 struct __align__(1024) Smem {
-    uint8_t q[kTile];
-    uint8_t k[KSTAGE][kTile];
-    uint8_t v[VSTAGE][kTile];
+    uint8_t q[Cfg<D>::kTile];
+    uint8_t k[KSTAGE][Cfg<D>::kTile];
+    uint8_t v[VSTAGE][Cfg<D>::kTile];
     uint64_t q_full;
     uint64_t k_full[KSTAGE], k_empty[KSTAGE];
     uint64_t v_full[VSTAGE], v_empty[VSTAGE];
@@ -98,15 +109,31 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     mbar_wait(bar, parity, &dummy);
 }
 
+// Loads one 128-row operand tile (D / 64 atoms) of a (rows, heads, D) tensor
+// starting at `row`, completing on `bar`.
+template <int D>
+__device__ __forceinline__ void tma_tile(uint8_t* dst, const CUtensorMap* m, uint64_t* bar, int head, int row) {
+#pragma unroll
+    for (int a = 0; a < Cfg<D>::kAtoms; ++a) tma_load_3d(dst + a * kAtom, m, bar, 64 * a, head, row);
+}
+
+template <int D>
 __global__ void __launch_bounds__(kThreads, 2)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const Params p) {
+    using C = Cfg<D>;
+    constexpr uint32_t kTile = C::kTile;
+    constexpr uint32_t cS = C::cS, cO = C::cO, cP = C::cP;
     extern __shared__ uint8_t smem_raw[];
-    // Two CTAs per SM only fit without alignment slack: the dynamic shared base
-    // (after the 1 KB the hardware reserves per CTA) must already be 1024-aligned
-    // for the 128-byte swizzle atoms.  Checked, never assumed.
-    Smem& S = *reinterpret_cast<Smem*>(smem_raw);
-    if (smem_u32(smem_raw) & 1023u) {
+    // Two CTAs per SM (d 64) only fit without alignment slack: the dynamic
+    // shared base (after the 1 KB the hardware reserves per CTA) must already
+    // be 1024-aligned for the 128-byte swizzle atoms -- checked, never assumed.
+    // At d 128 (one CTA per SM) the base is rounded up inside 1 KB of slack.
+    uint8_t* smem_al = C::kTwoPerSm ? smem_raw
+                                    : reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                                 ~uintptr_t(1023));
+    Smem<D>& S = *reinterpret_cast<Smem<D>*>(smem_al);
+    if (smem_u32(smem_al) & 1023u) {
         if (threadIdx.x == 0) raise_status(ATTN_SINK_DEV_LAYOUT);
         return;
     }
@@ -172,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(&S.tmem_base, kTmemCols);
+        tmem_alloc(&S.tmem_base, C::kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -200,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (is_k) {
                     prefetch_tmap(&tm_q);
                     mbar_expect_tx(&S.q_full, kTile);
-                    tma_load_3d(S.q, &tm_q, &S.q_full, 0, h, q_start + qs);
+                    tma_tile<D>(S.q, &tm_q, &S.q_full, h, q_start + qs);
                 }
             }
             // The one V tile that reaches past the request's last key (rows of the
@@ -220,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (!paged) {
                     if (lane == 0) {
                         mbar_expect_tx(bar, kTile);
-                        tma_load_3d(dst0 + st * kTile, tm, bar, 0, kvh, k_start + t * BN);
+                        tma_tile<D>(dst0 + st * kTile, tm, bar, kvh, k_start + t * BN);
                     }
                 } else {
                     // Segment `lane` covers keys j .. j + (1 << seg_shift) - 1, inside one page.
@@ -238,19 +265,21 @@ __global__ void __launch_bounds__(kThreads, 2)
                     for (int sg = 0; sg < nseg; ++sg) {
                         const int sl = __shfl_sync(0xffffffffu, slot, sg);
                         if (lane == 0)
-                            tma_load_3d(dst0 + st * kTile + ((uint32_t)sg << p.seg_shift) * 128u, tm, bar, 0, kvh,
-                                        sl);
+                            tma_tile<D>(dst0 + st * kTile + ((uint32_t)sg << p.seg_shift) * 128u, tm, bar, kvh, sl);
                     }
                 }
                 if (tail) {
                     // Used once per CTA (one tile holds the last key): parity 0.
                     tail_issued = true;
                     if (!__all_sync(0xffffffffu, mbar_wait(&S.v_tail, 0, abort))) break;
-                    // Key row r is the 128 bytes at r * 128 (the swizzle permutes
-                    // 16-byte chunks within a row), so rows Lk - t*BN .. BN - 1 are
-                    // one contiguous range.
-                    uint4* vt = reinterpret_cast<uint4*>(dst0 + st * kTile);
-                    for (int c = (Lk - t * BN) * 8 + lane; c < BN * 8; c += 32) vt[c] = make_uint4(0u, 0u, 0u, 0u);
+                    // Key row r of an atom is the 128 bytes at r * 128 (the swizzle
+                    // permutes 16-byte chunks within a row), so rows Lk - t*BN .. BN - 1
+                    // are one contiguous range per atom.
+#pragma unroll
+                    for (int a = 0; a < C::kAtoms; ++a) {
+                        uint4* vt = reinterpret_cast<uint4*>(dst0 + st * kTile + a * kAtom);
+                        for (int c = (Lk - t * BN) * 8 + lane; c < BN * 8; c += 32) vt[c] = make_uint4(0u, 0u, 0u, 0u);
+                    }
                     fence_proxy_async_smem();  // the tensor core reads the zeros through the async proxy
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&full[st]);
@@ -275,15 +304,18 @@ __global__ void __launch_bounds__(kThreads, 2)
             // Descriptor bases; a k-step adds its byte offset / 16 to the address field.
             const uint64_t dq = sdesc_sw128(smem_u32(S.q), 16, 1024);
             const uint64_t dk0 = sdesc_sw128(smem_u32(S.k[0]), 16, 1024);
-            const uint64_t dv0 = sdesc_sw128(smem_u32(S.v[0]), 8192, 1024);
+            const uint64_t dv0 = sdesc_sw128(smem_u32(S.v[0]), kAtom, 1024);  // MN atoms kAtom apart
             auto wait_all = [&](uint64_t* bar, uint32_t parity) {
                 return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
             };
             auto issue_S = [&](int it) {
                 const uint64_t dk = dk0 + (it % KSTAGE) * (kTile >> 4);
+                // 16 head-dim elements = 32 bytes per k-step; atom kk / 4
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)  // 16 head-dim elements = 32 bytes per k-step
-                    umma_ss_e(tmem + cS, dq + 2 * kk, dk + 2 * kk, idS, kk > 0);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t o = (kk >> 2) * (kAtom >> 4) + (kk & 3) * 2;
+                    umma_ss_e(tmem + cS, dq + o, dk + o, idS, kk > 0);
+                }
                 umma_commit_e(&S.s_full);
                 umma_commit_e(&S.k_empty[it % KSTAGE]);
             };
@@ -466,14 +498,14 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
                 rs = exps_half(H0{}, m_use) + exps_half(H1{}, m_use);
                 if (it > 0 && __any_sync(0xffffffffu, resc)) {
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) {
+#pragma unroll 1
+                    for (int ch = 0; ch < D / 32; ++ch) {
                         uint32_t o[32];
-                        tmem_ld32(tO + half * 32, o);
+                        tmem_ld32(tO + ch * 32, o);
                         tmem_ld_wait();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tmem_st32(tO + half * 32, o);
+                        tmem_st32(tO + ch * 32, o);
                     }
                 }
                 if (stored0) tmem_st_wait();  // the first half's earlier store lands before its rewrite
@@ -497,10 +529,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         const bool store = r < rows_valid && ok;
         uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)row * p.hq + h) * D);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        for (int ch = 0; ch < D / 32; ++ch) {
             uint32_t u[32];
             if (have) {  // warp-uniform: every lane takes part in the collective load
-                tmem_ld32(tO + half * 32, u);
+                tmem_ld32(tO + ch * 32, u);
                 tmem_ld_wait();
             } else {
 #pragma unroll
@@ -514,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     wv.y = pack_bf16x2(__uint_as_float(u[8 * c + 2]) * inv, __uint_as_float(u[8 * c + 3]) * inv);
                     wv.z = pack_bf16x2(__uint_as_float(u[8 * c + 4]) * inv, __uint_as_float(u[8 * c + 5]) * inv);
                     wv.w = pack_bf16x2(__uint_as_float(u[8 * c + 6]) * inv, __uint_as_float(u[8 * c + 7]) * inv);
-                    dst[half * 4 + c] = wv;
+                    dst[ch * 4 + c] = wv;
                 }
             }
         }
@@ -525,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, C::kTmemCols);
     }
 }
 
@@ -545,10 +577,12 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// (rows, heads, 64) bf16 tensor viewed as a 3-D map {d, head, row}; box {64, 1, box_rows}.
-// Rows are row_stride elements apart (0: heads * 64, i.e. contiguous).
-cudaError_t make_map(CUtensorMap* m, const void* base, int heads, long long rows, int box_rows,
+// (rows, heads, d) bf16 tensor viewed as a 3-D map {d, head, row}; box {64, 1,
+// box_rows}: one 128-byte-swizzled atom per copy (d / 64 copies per tile).
+// Rows are row_stride elements apart (0: heads * d, i.e. contiguous).
+cudaError_t make_map(CUtensorMap* m, const void* base, int d, int heads, long long rows, int box_rows,
                      std::string* what, long long row_stride = 0) {
+    const int D = d;
     auto fn = encode_fn();
     if (!fn) {
         *what = "cuTensorMapEncodeTiled unavailable";
@@ -556,7 +590,7 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int heads, long long rows
     }
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1)};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)(row_stride > 0 ? row_stride : (long long)D * heads) * 2};
-    cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)box_rows};
+    cuuint32_t box[3] = {64u, 1, (cuuint32_t)box_rows};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -568,8 +602,8 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int heads, long long rows
     return cudaSuccess;
 }
 
-cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s, std::string* what) {
-    if (a.total_q == 0) return cudaSuccess;
+template <int D>
+static cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s, std::string* what) {
     CUtensorMap tq, tk, tv;
     cudaError_t e;
     const bool paged = a.page_table != nullptr;
@@ -579,9 +613,9 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s, std::string* what) {
         seg_shift = page_shift < 7 ? page_shift : 7;  // segments of min(page_size, 128) rows
     }
     const long long krows = paged ? (long long)a.num_pages * a.page_size : a.total_k;
-    if ((e = make_map(&tq, a.q, a.hq, a.total_q, BM, what, a.q_rs)) != cudaSuccess) return e;
-    if ((e = make_map(&tk, a.k, a.hkv, krows, 1 << seg_shift, what, a.k_rs)) != cudaSuccess) return e;
-    if ((e = make_map(&tv, a.v, a.hkv, krows, 1 << seg_shift, what, a.v_rs)) != cudaSuccess) return e;
+    if ((e = make_map(&tq, a.q, D, a.hq, a.total_q, BM, what, a.q_rs)) != cudaSuccess) return e;
+    if ((e = make_map(&tk, a.k, D, a.hkv, krows, 1 << seg_shift, what, a.k_rs)) != cudaSuccess) return e;
+    if ((e = make_map(&tv, a.v, D, a.hkv, krows, 1 << seg_shift, what, a.v_rs)) != cudaSuccess) return e;
     Params p;
     p.page_table = a.page_table;
     p.seqlens_k = a.seqlens_k;
@@ -603,17 +637,23 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s, std::string* what) {
     p.win_last = a.win_last;
     p.causal = a.causal;
     p.scale_log2 = a.scale * ATTN_LOG2E;
-    const size_t smem = sizeof(Smem);
-    e = cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const size_t smem = sizeof(Smem<D>) + (Cfg<D>::kTwoPerSm ? 0 : 1024);
+    e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) {
         *what = "smem attribute";
         return e;
     }
     dim3 grid(a.hq, p.n_rt, a.batch);
-    fwd_kernel<<<grid, kThreads, smem, s>>>(tq, tk, tv, p);
+    fwd_kernel<D><<<grid, kThreads, smem, s>>>(tq, tk, tv, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) *what = "launch";
     return e;
+}
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s, std::string* what) {
+    if (a.total_q == 0) return cudaSuccess;
+    if (a.head_dim == 128) return launch_fwd_d<128>(a, s, what);
+    return launch_fwd_d<64>(a, s, what);
 }
 
 ATTN_DEFINE_STATUS_ACCESSOR(status_exchange)

@@ -62,9 +62,10 @@ def test_validation_without_gpu(lib):
     # window without causal is rejected
     rc = lib.attn_sink_fwd(P, P, P, None, P, P, 1, 8, 8, 4, 2, 64, 8, 8, 4, 8, 0, 0.0, P, None, None)
     assert rc == -1
-    # forward head_dim 128 unsupported
-    rc = lib.attn_sink_fwd(P, P, P, None, P, P, 1, 8, 8, 4, 2, 128, 8, 8, 0, 0, 1, 0.0, P, None, None)
+    # forward head_dim 96 unsupported (64 and 128 are)
+    rc = lib.attn_sink_fwd(P, P, P, None, P, P, 1, 8, 8, 4, 2, 96, 8, 8, 0, 0, 1, 0.0, P, None, None)
     assert rc == -2
+    assert b"64, 128" in lib.attn_sink_last_error()
     # dsink must accompany sink
     rc = lib.attn_sink_bwd(P, P, P, P, P, P, P, P, P, 1, 8, 8, 4, 2, 64, 8, 8, 0, 0, 1, 0.0, P, P, P, None, None)
     assert rc == -1
@@ -129,6 +130,6 @@ def test_validation_of_the_extended_entry_points_without_gpu(lib):
     assert b"start at 0" in lib.attn_sink_last_error()
     assert fwd_host([0, 5, 3], [0, 5, 9], 2) == -1
     assert b"non-decreasing" in lib.attn_sink_last_error()
-    assert fwd_host([0, 5], [0, 5], 1, head_dim=128) == -2
+    assert fwd_host([0, 5], [0, 5], 1, head_dim=96) == -2
     assert fwd_host([0], [0], 0) == 0
     assert fwd_host([0, 0, 0], [0, 7, 9], 2) == 0  # no query rows: nothing to do

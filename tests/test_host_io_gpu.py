@@ -18,9 +18,9 @@ def ext():
     return ext
 
 
-@pytest.mark.parametrize("pinned", [True, False])
-def test_fwd_host_equals_device_entry_point(ext, pinned):
-    p = wl.make_prefill(seqlens_q=[300, 0, 1, 129, 77], seqlens_k=[1000, 20, 1, 129, 400], hq=8, hkv=2, d=64,
+@pytest.mark.parametrize("pinned,d", [(True, 64), (False, 64), (True, 128)])
+def test_fwd_host_equals_device_entry_point(ext, pinned, d):
+    p = wl.make_prefill(seqlens_q=[300, 0, 1, 129, 77], seqlens_k=[1000, 20, 1, 129, 400], hq=8, hkv=2, d=d,
                         sink=(-2.0, 4.0), win_first=16, win_last=200, seed=3)
     host = {n: getattr(p, n) for n in ("q", "k", "v", "sink", "cu_seqlens_q", "cu_seqlens_k")}
     if pinned:
@@ -29,9 +29,10 @@ def test_fwd_host_equals_device_entry_point(ext, pinned):
                                           host["cu_seqlens_k"], p.win_first, p.win_last)
     torch.cuda.synchronize()
     assert ext.device_status() == 0
-    d = "cuda"
-    out_d, lse_d = ext.attn_sink_fwd(p.q.to(d), p.k.to(d), p.v.to(d), p.sink.to(d), p.cu_seqlens_q.to(d),
-                                     p.cu_seqlens_k.to(d), p.max_seqlen_q, p.max_seqlen_k, p.win_first, p.win_last)
+    dv = "cuda"
+    out_d, lse_d = ext.attn_sink_fwd(p.q.to(dv), p.k.to(dv), p.v.to(dv), p.sink.to(dv), p.cu_seqlens_q.to(dv),
+                                     p.cu_seqlens_k.to(dv), p.max_seqlen_q, p.max_seqlen_k, p.win_first,
+                                     p.win_last)
     torch.cuda.synchronize()
     assert torch.equal(out_h, out_d.cpu())
     assert torch.equal(lse_h, lse_d.cpu())

@@ -18,8 +18,8 @@ def ext():
     return ext
 
 
-def _problem(hq, hkv, seqlens=(300, 129, 1), seed=31, with_dout=False):
-    return wl.make_prefill(seqlens_q=list(seqlens), hq=hq, hkv=hkv, d=64, sink="normal", causal=True,
+def _problem(hq, hkv, seqlens=(300, 129, 1), seed=31, with_dout=False, d=64):
+    return wl.make_prefill(seqlens_q=list(seqlens), hq=hq, hkv=hkv, d=d, sink="normal", causal=True,
                            with_dout=with_dout, seed=seed)
 
 
@@ -27,9 +27,9 @@ def _pack(p):
     return torch.cat([p.q, p.k, p.v], dim=1).contiguous()  # (T, hq + 2 hkv, d)
 
 
-@pytest.mark.parametrize("hq,hkv", [(8, 2), (4, 4)])
-def test_fwd_qkvpacked_equals_separate(ext, hq, hkv):
-    p = _problem(hq, hkv)
+@pytest.mark.parametrize("hq,hkv,d", [(8, 2, 64), (4, 4, 64), (8, 2, 128)])
+def test_fwd_qkvpacked_equals_separate(ext, hq, hkv, d):
+    p = _problem(hq, hkv, d=d)
     dev = "cuda"
     qkv = _pack(p).to(dev)
     cq = p.cu_seqlens_q.to(dev)

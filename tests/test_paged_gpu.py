@@ -132,10 +132,11 @@ FWD_CASES = {
 }
 
 
-@pytest.mark.parametrize("name", list(FWD_CASES))
-def test_fwd_paged_matches_oracle(ext, name):
+@pytest.mark.parametrize("name,d", [(n, 64) for n in FWD_CASES] +
+                         [(n, 128) for n in ("ps16_append", "ps8_prefilled", "ps32_first_last")])
+def test_fwd_paged_matches_oracle(ext, name, d):
     sq, sk, hq, hkv, ps, sink, F_, W, append = FWD_CASES[name]
-    pe = wl.make_paged_extend(seqlens_q=sq, seqlens_k=sk, hq=hq, hkv=hkv, d=64, page_size=ps, sink=sink,
+    pe = wl.make_paged_extend(seqlens_q=sq, seqlens_k=sk, hq=hq, hkv=hkv, d=d, page_size=ps, sink=sink,
                               win_first=F_, win_last=W, seed=13, extra_pages=4)
     kw, vw = orc.kv_append(pe.k_cache, pe.v_cache, pe.page_table, pe.seqlens_k, pe.k_new, pe.v_new, ps,
                            cu_new=pe.cu_seqlens_q)

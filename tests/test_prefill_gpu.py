@@ -64,6 +64,35 @@ def test_fwd_matches_oracle(ext, name):
     assert_lse_close(lse, LSE, what=name)
 
 
+# head_dim 128 (one CTA per SM, two 64-wide swizzle atoms per operand row):
+# the window run of sglang PR "To implement attention-sink" serves a model with
+# 128-wide heads (Qwen3-8B: 32 query heads over 8 KV heads).
+D128_CASES = ["square_gqa2", "ragged_extend", "odd_group", "non_causal", "window_small", "window_1024_7168",
+              "sliding_only", "more_q_than_k", "long_prefix"]
+
+
+@pytest.mark.parametrize("name", D128_CASES)
+def test_fwd_d128_matches_oracle(ext, name):
+    sq, sk, hq, hkv, sink, F_, W, causal = CASES[name]
+    p = wl.make_prefill(seqlens_q=sq, seqlens_k=sk, hq=hq, hkv=hkv, d=128, sink=sink,
+                        win_first=F_, win_last=W, causal=causal, seed=12)
+    out, lse = run_fwd(ext, p)
+    O, LSE = oracle_fwd(p)
+    assert_out_close(out, O, what=name)
+    assert_lse_close(lse, LSE, what=name)
+
+
+def test_fwd_d128_gqa4_window(ext):
+    """The 128-wide-head shape of the window run (4 query heads per KV head) with
+    the first 1024 + last 7168 window over 9000 keys."""
+    p = wl.make_prefill(seqlens_q=[300, 129], seqlens_k=[9000, 2000], hq=8, hkv=2, d=128, sink=None,
+                        win_first=1024, win_last=7168, causal=True, seed=21)
+    out, lse = run_fwd(ext, p)
+    O, LSE = oracle_fwd(p)
+    assert_out_close(out, O)
+    assert_lse_close(lse, LSE)
+
+
 @pytest.mark.parametrize("sig", [-math.inf, 80.0, math.inf])
 def test_fwd_sink_limits(ext, sig):
     p = wl.make_prefill(seqlens_q=[150, 40], hq=4, hkv=2, d=64, sink="normal", seed=3)

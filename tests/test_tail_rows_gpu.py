@@ -58,8 +58,9 @@ def test_fwd_paged_ignores_unowned_slots(ext, page_size, win):
     assert torch.equal(results[0][1], results[1][1])
 
 
-def test_fwd_neighbour_and_trailing_rows_do_not_leak(ext):
-    p = wl.make_prefill(seqlens_q=[100, 77, 129], seqlens_k=[300, 200, 129], hq=8, hkv=2, d=64, sink="normal",
+@pytest.mark.parametrize("d", [64, 128])
+def test_fwd_neighbour_and_trailing_rows_do_not_leak(ext, d):
+    p = wl.make_prefill(seqlens_q=[100, 77, 129], seqlens_k=[300, 200, 129], hq=8, hkv=2, d=d, sink="normal",
                         seed=23)
     cq, ck = p.cu_seqlens_q.tolist(), p.cu_seqlens_k.tolist()
     dev = "cuda"
