@@ -97,7 +97,7 @@ enum {
  *   win_first, win_last          window selection (needs causal = 1)
  *   out          (total_q, hq, head_dim) bf16
  *   lse          (hq, total_q) fp32, natural log, includes the sink; may be NULL
- * Supported: head_dim 64; hq % hkv == 0.  A request's results depend on its
+ * Supported: head_dim 64 or 128; hq % hkv == 0.  A request's results depend on its
  * own rows only: the value rows that its last key tile covers past its last
  * key (another request's, or beyond cu_seqlens_k[batch]) are replaced by zeros
  * in shared memory, so they may hold anything, NaN included.
@@ -250,7 +250,7 @@ int attn_sink_decode_paged_append(const attn_bf16* q, const attn_bf16* k_new, co
  * pageable buffers still give correct results, without overlap.  Returns once
  * the work is queued; `stream` waits for all of it (synchronise `stream`
  * before reading out / lse).  Device scratch for the whole batch comes from the
- * library's stream-ordered pool.  Supported: head_dim 64; hq % hkv == 0.
+ * library's stream-ordered pool.  Supported: head_dim 64 or 128; hq % hkv == 0.
  */
 int attn_sink_fwd_host(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v,
                        const float* sink, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
@@ -276,7 +276,7 @@ int attn_sink_fwd_host(const attn_bf16* q, const attn_bf16* k, const attn_bf16* 
  *   seqlens_k    (batch,) int32 device, prefix + chunk
  *   max_seqlen_q, max_seqlen_k   host upper bounds (grid sizing, append grid)
  *   sink, win_first, win_last, causal, scale, out, lse: as in attn_sink_fwd
- * Supported: head_dim 64; hq % hkv == 0; page_size a power of two >= 8
+ * Supported: head_dim 64 or 128; hq % hkv == 0; page_size a power of two >= 8
  * (a 128-key tile is then one TMA copy per page segment).  Cache slots that a
  * request does not own (the rest of its last page, any other page) never
  * reach its results and may hold anything, NaN included.
@@ -303,7 +303,9 @@ int attn_sink_fwd_paged(const attn_bf16* q, const attn_bf16* k_new, const attn_b
  *                of each KV head)
  *   dsink        (hq,) fp32; must be non-NULL iff sink is non-NULL; written
  *                (not accumulated)
- * Supported: head_dim 64; hq % hkv == 0.  A request's gradients depend on
+ * Supported: head_dim 64 or 128 (at 128 the main kernel runs in two passes,
+ * each recomputing S and dP and producing 64 columns of dq, dk, dv);
+ * hq % hkv == 0.  A request's gradients depend on
  * its own rows only: the rows that its last query or key tile covers past its
  * own (another request's, or past total_q / total_k) are replaced by zeros in
  * shared memory, so they may hold anything, NaN included.

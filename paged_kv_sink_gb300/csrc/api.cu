@@ -506,7 +506,7 @@ int bwd_impl(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, const l
              int max_seqlen_q, int max_seqlen_k, int win_first, int win_last, int causal, float scale,
              attn_bf16* dq, attn_bf16* dk, attn_bf16* dv, float* dsink, void* stream) {
     int rc = validate_varlen("bwd", q, k, v, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, hq, hkv, head_dim,
-                             max_seqlen_q, max_seqlen_k, win_first, win_last, causal, false);
+                             max_seqlen_q, max_seqlen_k, win_first, win_last, causal, true);
     if (rc != ATTN_SINK_OK) return rc;
     if ((sink == nullptr) != (dsink == nullptr))
         return fail(ATTN_SINK_ERR_INVALID, "bwd: dsink must be given exactly when sink is");

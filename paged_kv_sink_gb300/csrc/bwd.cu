@@ -36,24 +36,37 @@ using namespace sm103;
 
 constexpr int BM = 128;  // query rows per tile
 constexpr int BN = 128;  // keys per CTA
-constexpr int D = 64;
+constexpr int DH = 64;   // output columns of dQ / dK / dV per main-kernel pass
 constexpr int kThreads = 384;
 constexpr int kRegsCtrl = 104;
 constexpr int kRegsWork = 200;  // 128*104 + 256*200 = 64512 = 384 * 168
 constexpr int kWork = 256;      // elementwise threads: warps 4..11
-constexpr int kQStages = 3;     // Q / dO ring depth
-constexpr uint32_t kTile = 128 * 128;
+constexpr uint32_t kTile = 128 * 128;  // one 128-byte-swizzled atom: 128 rows x 128 bytes
+// Head-dim dependent sizes.  A 128-row operand tile of Q, dO, K or V is D / 64
+// atoms (atom a: elements 64a .. 64a + 63 of every row, at byte offset
+// a * kTile).  At d 128 the products S and dP run over both atoms, and the main
+// kernel runs twice, each pass producing one 64-column half of dQ, dK and dV
+// (the TMEM budget -- S, dP, dV, dK, dQ and dS -- fits 64 output columns); the
+// Q / dO ring then has one stage to fit shared memory.
+template <int D>
+struct Cfg {
+    static constexpr int kAtoms = D / 64;
+    static constexpr uint32_t kOp = kTile * kAtoms;
+    static constexpr int kQStages = D == 64 ? 3 : 1;
+};
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: S, dP (fp32), dV, dK (fp32 accumulators over the whole loop),
 // dQ (fp32, one step) and dS (bf16 pairs: column c holds keys 2c and 2c+1), the
 // A operand of dQ = dS K read straight from TMEM.
 constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDK = 320, cDQ = 384, cDS = 448;
 
+template <int D>
 struct __align__(1024) Smem {
-    uint8_t k[kTile];
-    uint8_t v[kTile];
-    uint8_t q[kQStages][kTile];
-    uint8_t dout[kQStages][kTile];
+    static constexpr int kQStages = Cfg<D>::kQStages;
+    uint8_t k[Cfg<D>::kOp];
+    uint8_t v[Cfg<D>::kOp];
+    uint8_t q[kQStages][Cfg<D>::kOp];
+    uint8_t dout[kQStages][Cfg<D>::kOp];
     uint8_t pb[2 * kTile];   // P  (128 queries x 128 keys): two 64-key atoms of 128-byte rows
     uint8_t dsb[2 * kTile];  // dS (same layout)
     uint8_t dq_stage[2][kTile];  // dQ tile staging: two 32-column fp32 halves, 128-byte swizzled rows
@@ -75,14 +88,22 @@ struct MainParams {
     const int32_t* cu_k;
     const float* lse;      // (hq, total_q)
     const float* dvec;     // (hq, total_q)
-    float* dq_accum;       // (total_q, hq, D) fp32
-    __nv_bfloat16* dk;     // (total_k, hkv, D), rows dk_rs elements apart
+    float* dq_accum;       // (total_q, hq, d) fp32
+    __nv_bfloat16* dk;     // (total_k, hkv, d), rows dk_rs elements apart
     __nv_bfloat16* dv;     // rows dv_rs elements apart
     long long dk_rs, dv_rs;
     int hq, hkv, group, total_q, total_k;
     int win_first, win_last, causal;
     float scale, scale_log2;
+    int dhalf;  // output columns 64 * dhalf .. + 63 of dQ, dK, dV (d 128: two passes)
 };
+
+// Loads one 128-row operand tile (D / 64 atoms) starting at `row`.
+template <int D>
+__device__ __forceinline__ void tma_tile(uint8_t* dst, const CUtensorMap* m, uint64_t* bar, int head, int row) {
+#pragma unroll
+    for (int a = 0; a < Cfg<D>::kAtoms; ++a) tma_load_3d(dst + a * kTile, m, bar, 64 * a, head, row);
+}
 
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     int dummy = 0;
@@ -139,12 +160,16 @@ __device__ __forceinline__ void p_ds_half(const uint32_t (&sr)[32], const uint32
     }
 }
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_dq, const MainParams p) {
+    using C = Cfg<D>;
+    constexpr int kQStages = C::kQStages;
+    constexpr uint32_t kOp = C::kOp;
     extern __shared__ uint8_t smem_raw[];
-    Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Smem<D>& S = *reinterpret_cast<Smem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Grid (KV head, request, key tile) with the key tile slowest: causal key
     // tile 0 is seen by every query tile, so launching tiles in increasing order
@@ -210,17 +235,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             // (key row r and query row r are the 128 bytes at r * 128, so they
             // form one contiguous range whatever the swizzle).
             auto zero_rows = [&](uint8_t* tile, int r0) {
-                uint4* t4 = reinterpret_cast<uint4*>(tile);
-                for (int c = r0 * 8 + lane; c < BM * 8; c += 32) t4[c] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int a = 0; a < C::kAtoms; ++a) {
+                    uint4* t4 = reinterpret_cast<uint4*>(tile + a * kTile);
+                    for (int c = r0 * 8 + lane; c < BM * 8; c += 32) t4[c] = make_uint4(0u, 0u, 0u, 0u);
+                }
             };
             if (lane == 0) {
                 prefetch_tmap(&tm_q);
                 prefetch_tmap(&tm_k);
                 prefetch_tmap(&tm_v);
                 prefetch_tmap(&tm_do);
-                mbar_expect_tx(&S.kv_full, 2 * kTile);
-                tma_load_3d(S.k, &tm_k, &S.kv_full, 0, kvh, k_start + j0);
-                tma_load_3d(S.v, &tm_v, &S.kv_full, 0, kvh, k_start + j0);
+                mbar_expect_tx(&S.kv_full, 2 * kOp);
+                tma_tile<D>(S.k, &tm_k, &S.kv_full, kvh, k_start + j0);
+                tma_tile<D>(S.v, &tm_v, &S.kv_full, kvh, k_start + j0);
             }
             bool ok = true;
             if (kv_tail) {
@@ -245,9 +273,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool tail = q0 + BM > Lq;
                 uint64_t* bar = tail ? &S.qdo_tail : &S.qdo_full[st];
                 if (lane == 0) {
-                    mbar_expect_tx(bar, 2 * kTile);
-                    tma_load_3d(S.q[st], &tm_q, bar, 0, h, q_start + q0);
-                    tma_load_3d(S.dout[st], &tm_do, bar, 0, h, q_start + q0);
+                    mbar_expect_tx(bar, 2 * kOp);
+                    tma_tile<D>(S.q[st], &tm_q, bar, h, q_start + q0);
+                    tma_tile<D>(S.dout[st], &tm_do, bar, h, q_start + q0);
                 }
                 if (tail) {
                     tail_pending = true;
@@ -285,8 +313,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     const int hh = kvh * p.group + g_c;
                     const int qq0 = (qr.lo + qt_c) * BM;
-                    tma_reduce_add_3d(&tm_dq, S.dq_stage[0], 0, hh, q_start + qq0);
-                    tma_reduce_add_3d(&tm_dq, S.dq_stage[1], 32, hh, q_start + qq0);
+                    tma_reduce_add_3d(&tm_dq, S.dq_stage[0], p.dhalf * DH, hh, q_start + qq0);
+                    tma_reduce_add_3d(&tm_dq, S.dq_stage[1], p.dhalf * DH + 32, hh, q_start + qq0);
                     bulk_commit_group();
                     bulk_wait_read_all();
                     mbar_arrive(&S.dq_stage_free);
@@ -309,12 +337,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // and within a stream the independent accumulator chains are
             // interleaved k-step by k-step.
             constexpr uint32_t idSS = idesc_bf16_f32(BM, BN, false, false);  // S, dP: both K-major
-            constexpr uint32_t idKV = idesc_bf16_f32(BN, D, true, true);     // dV, dK: A (P^T, dS^T) MN-major
-            constexpr uint32_t idQ = idesc_bf16_f32(BM, D, false, true);     // dQ: A (dS) K-major, B (K) MN-major
+            constexpr uint32_t idKV = idesc_bf16_f32(BN, DH, true, true);    // dV, dK: A (P^T, dS^T) MN-major
+            constexpr uint32_t idQ = idesc_bf16_f32(BM, DH, false, true);    // dQ: A (dS) K-major, B (K) MN-major
+            const uint32_t half_off = (uint32_t)p.dhalf * (kTile >> 4);      // this pass's 64-column atom
             // Descriptor bases; a k-step adds its byte offset / 16 to the address field.
             const uint64_t dk_k = sdesc_sw128(smem_u32(S.k), 16, 1024);        // K, K-major (B of S)
             const uint64_t dv_k = sdesc_sw128(smem_u32(S.v), 16, 1024);        // V, K-major (B of dP)
-            const uint64_t dk_mn = sdesc_sw128(smem_u32(S.k), 8192, 1024);     // K, MN-major (B of dQ)
+            const uint64_t dk_mn = sdesc_sw128(smem_u32(S.k), 8192, 1024) + half_off;  // K, MN-major (B of dQ)
             const uint64_t dp_mn = sdesc_sw128(smem_u32(S.pb), kTile, 1024);   // P^T, MN-major (A of dV)
             const uint64_t ds_mn = sdesc_sw128(smem_u32(S.dsb), kTile, 1024);  // dS^T, MN-major (A of dK)
             auto wait_all = [&](uint64_t* bar, uint32_t parity) {
@@ -331,8 +360,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t ddo_k = sdesc_sw128(smem_u32(S.dout[st]), 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {  // 16 head-dim elements = 32 bytes per k-step
-                        umma_ss_e(tmem + cS, dq_k + 2 * kk, dk_k + 2 * kk, idSS, kk > 0);
-                        umma_ss_e(tmem + cDP, ddo_k + 2 * kk, dv_k + 2 * kk, idSS, kk > 0);
+                        const uint32_t o = (kk >> 2) * (kTile >> 4) + (kk & 3) * 2;  // atom kk / 4
+                        umma_ss_e(tmem + cS, dq_k + o, dk_k + o, idSS, kk > 0);
+                        umma_ss_e(tmem + cDP, ddo_k + o, dv_k + o, idSS, kk > 0);
                     }
                     umma_commit_e(&S.sdp_full);
                 }
@@ -345,8 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // pds_full also means the previous dQ has been read out of TMEM
                     if (!(ok = wait_all(&S.pds_full, t & 1))) break;
                     tc_fence_after();
-                    const uint64_t dq_mn = sdesc_sw128(smem_u32(S.q[st]), 8192, 1024);
-                    const uint64_t ddo_mn = sdesc_sw128(smem_u32(S.dout[st]), 8192, 1024);
+                    const uint64_t dq_mn = sdesc_sw128(smem_u32(S.q[st]), 8192, 1024) + half_off;
+                    const uint64_t ddo_mn = sdesc_sw128(smem_u32(S.dout[st]), 8192, 1024) + half_off;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         // dV / dK: k-step kk runs over query rows 16 kk .. 16 kk + 15 of P / dS
@@ -530,7 +560,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool have = ok && T > 0;
         if (have) tc_fence_after();
         const int kpos = j0 + i;
-        const size_t rowoff = (size_t)(k_start + kpos) * (size_t)(ch == 0 ? p.dk_rs : p.dv_rs) + (size_t)kvh * D;
+        const size_t rowoff =
+            (size_t)(k_start + kpos) * (size_t)(ch == 0 ? p.dk_rs : p.dv_rs) + (size_t)kvh * D + p.dhalf * DH;
         const uint32_t col = ch == 0 ? cDK : cDV;
         const float f = 1.f;  // dK: the scale rides on dS
         __nv_bfloat16* outp = ch == 0 ? p.dk : p.dv;
@@ -571,6 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // D_i = rowsum(dO_i o O_i) and dsink.  Block: 256 threads, 64 rows of one head;
 // 8 threads per row, 16 bytes each.
 
+template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ out,
                                                              const __nv_bfloat16* __restrict__ dout,
                                                              const float* __restrict__ lse,
@@ -589,12 +621,16 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
         const int row = blockIdx.x * 64 + rr * 32 + (tid >> 3);
         float d = 0.f;
         if (row < rows) {
-            const size_t base = ((size_t)row * hq + h) * D + sub * 8;
-            const uint4 o = *reinterpret_cast<const uint4*>(out + base);
-            const uint4 g = *reinterpret_cast<const uint4*>(dout + base);
-            d = bf16_lo(o.x) * bf16_lo(g.x) + bf16_hi(o.x) * bf16_hi(g.x) + bf16_lo(o.y) * bf16_lo(g.y) +
-                bf16_hi(o.y) * bf16_hi(g.y) + bf16_lo(o.z) * bf16_lo(g.z) + bf16_hi(o.z) * bf16_hi(g.z) +
-                bf16_lo(o.w) * bf16_lo(g.w) + bf16_hi(o.w) * bf16_hi(g.w);
+            // eight threads per row, D / 8 elements each (16-byte loads)
+#pragma unroll
+            for (int j = 0; j < D / 64; ++j) {
+                const size_t base = ((size_t)row * hq + h) * D + j * 64 + sub * 8;
+                const uint4 o = *reinterpret_cast<const uint4*>(out + base);
+                const uint4 g = *reinterpret_cast<const uint4*>(dout + base);
+                d += bf16_lo(o.x) * bf16_lo(g.x) + bf16_hi(o.x) * bf16_hi(g.x) + bf16_lo(o.y) * bf16_lo(g.y) +
+                     bf16_hi(o.y) * bf16_hi(g.y) + bf16_lo(o.z) * bf16_lo(g.z) + bf16_hi(o.z) * bf16_hi(g.z) +
+                     bf16_lo(o.w) * bf16_lo(g.w) + bf16_hi(o.w) * bf16_hi(g.w);
+            }
         }
         d += __shfl_xor_sync(0xffffffffu, d, 1);
         d += __shfl_xor_sync(0xffffffffu, d, 2);
@@ -640,12 +676,12 @@ __global__ void bwd_dq_convert_kernel(const float4* __restrict__ acc, uint2* __r
 // ---------------------------------------------------------------------------
 // Host side
 
-cudaError_t make_map(CUtensorMap* m, const void* base, int heads, long long rows, std::string* what,
+cudaError_t make_map(CUtensorMap* m, const void* base, int d, int heads, long long rows, std::string* what,
                      long long row_stride = 0);
-cudaError_t make_map_dq(CUtensorMap* m, const float* base, int heads, long long rows, std::string* what);
+cudaError_t make_map_dq(CUtensorMap* m, const float* base, int d, int heads, long long rows, std::string* what);
 
 size_t workspace_bytes(const Args& a) {
-    const size_t acc = (size_t)a.total_q * a.hq * D * sizeof(float);
+    const size_t acc = (size_t)a.total_q * a.hq * a.head_dim * sizeof(float);
     const size_t dv = (size_t)a.hq * a.total_q * sizeof(float);
     return ((acc + 255) & ~size_t(255)) + dv;
 }
@@ -663,7 +699,9 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-cudaError_t make_map(CUtensorMap* m, const void* base, int heads, long long rows, std::string* what,
+// (rows, heads, d) bf16 tensor as {d, head, row}; box {64, 1, 128}: one
+// 128-byte-swizzled atom per copy.
+cudaError_t make_map(CUtensorMap* m, const void* base, int D, int heads, long long rows, std::string* what,
                      long long row_stride) {
     auto fn = encode_fn();
     if (!fn) {
@@ -672,7 +710,7 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int heads, long long rows
     }
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1)};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)(row_stride > 0 ? row_stride : (long long)D * heads) * 2};
-    cuuint32_t box[3] = {(cuuint32_t)D, 1, 128};
+    cuuint32_t box[3] = {64u, 1, 128};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -684,8 +722,8 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int heads, long long rows
     return cudaSuccess;
 }
 
-// (rows, heads, 64) fp32 dQ accumulator as {d, head, row}; box {32, 1, 128}, 128-byte swizzle.
-cudaError_t make_map_dq(CUtensorMap* m, const float* base, int heads, long long rows, std::string* what) {
+// (rows, heads, d) fp32 dQ accumulator as {d, head, row}; box {32, 1, 128}, 128-byte swizzle.
+cudaError_t make_map_dq(CUtensorMap* m, const float* base, int D, int heads, long long rows, std::string* what) {
     auto fn = encode_fn();
     if (!fn) {
         *what = "cuTensorMapEncodeTiled unavailable";
@@ -705,8 +743,8 @@ cudaError_t make_map_dq(CUtensorMap* m, const float* base, int heads, long long 
     return cudaSuccess;
 }
 
-cudaError_t launch(const Args& a, void* workspace, size_t ws_bytes, cudaStream_t s, std::string* what) {
-    if (a.total_q == 0 && a.total_k == 0) return cudaSuccess;
+template <int D>
+static cudaError_t launch_d(const Args& a, void* workspace, cudaStream_t s, std::string* what) {
     cudaError_t e;
     const size_t acc_bytes = (size_t)a.total_q * a.hq * D * sizeof(float);
     float* dq_accum = static_cast<float*>(workspace);
@@ -729,7 +767,7 @@ cudaError_t launch(const Args& a, void* workspace, size_t ws_bytes, cudaStream_t
             return e;
         }
         dim3 g1((a.total_q + 63) / 64, a.hq);
-        bwd_preprocess_kernel<<<g1, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(a.out),
+        bwd_preprocess_kernel<D><<<g1, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(a.out),
                                                  reinterpret_cast<const __nv_bfloat16*>(a.dout), a.lse, a.sink,
                                                  dvec, a.dsink, a.total_q, a.hq, a.cu_q, a.batch);
         if ((e = cudaGetLastError()) != cudaSuccess) {
@@ -739,11 +777,11 @@ cudaError_t launch(const Args& a, void* workspace, size_t ws_bytes, cudaStream_t
     }
     if (a.total_q > 0 && a.total_k > 0 && a.max_seqlen_k > 0) {
         CUtensorMap tq, tk, tv, tdo, tdq;
-        if ((e = make_map(&tq, a.q, a.hq, a.total_q, what, a.q_rs)) != cudaSuccess) return e;
-        if ((e = make_map(&tk, a.k, a.hkv, a.total_k, what, a.k_rs)) != cudaSuccess) return e;
-        if ((e = make_map(&tv, a.v, a.hkv, a.total_k, what, a.v_rs)) != cudaSuccess) return e;
-        if ((e = make_map(&tdo, a.dout, a.hq, a.total_q, what)) != cudaSuccess) return e;
-        if ((e = make_map_dq(&tdq, dq_accum, a.hq, a.total_q, what)) != cudaSuccess) return e;
+        if ((e = make_map(&tq, a.q, D, a.hq, a.total_q, what, a.q_rs)) != cudaSuccess) return e;
+        if ((e = make_map(&tk, a.k, D, a.hkv, a.total_k, what, a.k_rs)) != cudaSuccess) return e;
+        if ((e = make_map(&tv, a.v, D, a.hkv, a.total_k, what, a.v_rs)) != cudaSuccess) return e;
+        if ((e = make_map(&tdo, a.dout, D, a.hq, a.total_q, what)) != cudaSuccess) return e;
+        if ((e = make_map_dq(&tdq, dq_accum, D, a.hq, a.total_q, what)) != cudaSuccess) return e;
         MainParams p;
         p.cu_q = a.cu_q;
         p.cu_k = a.cu_k;
@@ -764,17 +802,20 @@ cudaError_t launch(const Args& a, void* workspace, size_t ws_bytes, cudaStream_t
         p.causal = a.causal;
         p.scale = a.scale;
         p.scale_log2 = a.scale * ATTN_LOG2E;
-        const size_t smem = sizeof(Smem) + 1024;
-        if ((e = cudaFuncSetAttribute(bwd_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-            cudaSuccess) {
+        const size_t smem = sizeof(Smem<D>) + 1024;
+        if ((e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)smem)) != cudaSuccess) {
             *what = "smem attribute";
             return e;
         }
         dim3 g2(a.hkv, a.batch, (a.max_seqlen_k + BN - 1) / BN);
-        bwd_main_kernel<<<g2, kThreads, smem, s>>>(tq, tk, tv, tdo, tdq, p);
-        if ((e = cudaGetLastError()) != cudaSuccess) {
-            *what = "main launch";
-            return e;
+        for (int half = 0; half < D / DH; ++half) {  // one pass per 64 output columns
+            p.dhalf = half;
+            bwd_main_kernel<D><<<g2, kThreads, smem, s>>>(tq, tk, tv, tdo, tdq, p);
+            if ((e = cudaGetLastError()) != cudaSuccess) {
+                *what = "main launch";
+                return e;
+            }
         }
     }
     if (a.total_q > 0) {
@@ -790,6 +831,15 @@ cudaError_t launch(const Args& a, void* workspace, size_t ws_bytes, cudaStream_t
         }
     }
     return cudaSuccess;
+}
+
+cudaError_t launch(const Args& a, void* workspace, size_t ws_bytes, cudaStream_t s, std::string* what) {
+    if (a.total_q == 0 && a.total_k == 0) return cudaSuccess;
+    if (ws_bytes < workspace_bytes(a)) {
+        *what = "workspace too small";
+        return cudaErrorInvalidValue;
+    }
+    return a.head_dim == 128 ? launch_d<128>(a, workspace, s, what) : launch_d<64>(a, workspace, s, what);
 }
 
 ATTN_DEFINE_STATUS_ACCESSOR(status_exchange)

@@ -70,9 +70,10 @@ def test_fwd_kvpacked_equals_separate(ext):
     assert torch.equal(out_p.cpu(), out_s.cpu()) and torch.equal(lse_p.cpu(), lse_s.cpu())
 
 
-def test_bwd_qkvpacked(ext):
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_qkvpacked(ext, d):
     hq, hkv = 8, 2
-    p = _problem(hq, hkv, seqlens=(300, 129), with_dout=True)
+    p = _problem(hq, hkv, seqlens=(300, 129), with_dout=True, d=d)
     dev = "cuda"
     qkv = _pack(p).to(dev)
     cq = p.cu_seqlens_q.to(dev)

@@ -101,10 +101,11 @@ def _rel(a, b):
     return float((a - b).norm() / max(float(b.norm()), 1e-30))
 
 
-def test_bwd_trailing_rows_do_not_leak(ext):
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_trailing_rows_do_not_leak(ext, d):
     """64 NaN rows past the end of q, dout, k and v (the last request's tail tiles
     read them): every gradient, dsink included, is unchanged."""
-    p = wl.make_prefill(seqlens_q=[100, 77, 129], seqlens_k=[300, 200, 129], hq=8, hkv=2, d=64, sink="normal",
+    p = wl.make_prefill(seqlens_q=[100, 77, 129], seqlens_k=[300, 200, 129], hq=8, hkv=2, d=d, sink="normal",
                         with_dout=True, seed=29)
     res = []
     for poison in (False, True):
