@@ -246,16 +246,17 @@ def bench_extend(torch, ext, dev, p, steps, warmup, flush, peaks, peak_src, sync
     lse = torch.empty((p.hq, q.shape[0]), dtype=torch.float32, device=dev)
 
     def step():
-        ext.attn_sink_fwd(q, k, v, sink, cq, ck, p.max_seqlen_q, p.max_seqlen_k, out=out, lse=lse)
+        ext.attn_sink_fwd(q, k, v, sink, cq, ck, p.max_seqlen_q, p.max_seqlen_k, p.win_first, p.win_last,
+                          out=out, lse=lse)
 
     times = time_steps(torch, step, steps, warmup, flush, sync)
-    flops = fwd_flops(p)
+    flops = fwd_flops(p)  # visible (query, key) pairs only: keys a window skips are work avoided
     ms = sum(times) / len(times)
     achieved = flops / (ms * 1e-3) / 1e12
     roof = {"kernel": "attn::prefill::fwd_kernel", "bound": "tensor", "achieved": achieved,
             "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
             "peak_source": f"bf16 burst, {peak_src}",
-            "traffic": _traffic("fwd_kernel/extend_varlen", "prefill_fwd.cu"),
+            "traffic": _traffic("fwd_kernel/" + p.name.split()[0], "prefill_fwd.cu"),
             "algorithmic_flops_per_launch": flops}
     return ms, flops, roof, times
 
@@ -510,7 +511,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the decode / training workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
     ap.add_argument("--only", default=None,
-                    choices=["decode_sink", "decode_window", "train", "extend_paged", "decode_append"],
+                    choices=["decode_sink", "decode_window", "train", "extend_paged", "decode_append",
+                             "extend_window"],
                     help="run one secondary workload alone and print its line (for profiling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -546,6 +548,10 @@ def main():
             r = bench_extend_paged(torch, ext, dev, w, args.steps, args.warmup, flush, peaks, peak_src)
         elif args.only == "decode_append":
             r = bench_decode_append(torch, ext, dev, w, args.steps, args.warmup, flush, peaks, peak_src)
+        elif args.only == "extend_window":
+            ms, flops, roof, _ = bench_extend(torch, ext, dev, w, args.steps, args.warmup, flush, peaks, peak_src)
+            r = {"metric": "attn TFLOP/s (visible pairs)", "value": roof["achieved"], "unit": "TFLOP/s",
+                 "ms_per_step": ms, "algorithmic_tflop_per_step": flops / 1e12, "roofline": roof}
         else:
             r = bench_decode(torch, ext, dev, w, args.steps, args.warmup, flush, peaks, peak_src)
         check_status(ext, args.only)
@@ -583,6 +589,15 @@ def main():
                                      peak_src)
         check_status(ext, "train")
         del tr
+        pw = wl.workload("extend_window", seed=0)
+        ms_w, flops_w, roof_w, _ = bench_extend(torch, ext, dev, pw, max(3, args.steps // 2), args.warmup, flush,
+                                                peaks, peak_src)
+        check_status(ext, "extend_window")
+        extra["extend_window"] = {"metric": "attn TFLOP/s (visible pairs)", "value": roof_w["achieved"],
+                                  "unit": "TFLOP/s", "ms_per_step": ms_w,
+                                  "algorithmic_tflop_per_step": flops_w / 1e12, "workload": pw.name,
+                                  "roofline": roof_w}
+        del pw
         pe = wl.workload("extend_paged", seed=0)
         extra["extend_paged"] = bench_extend_paged(torch, ext, dev, pe, max(3, args.steps // 2), args.warmup,
                                                    flush, peaks, peak_src)

@@ -21,6 +21,11 @@ Workloads (shapes from the two forms of the sink described on the pages):
   d 128, page 64, L U{8192..65536}.
 * ``train``          -- training forward+backward with sink: B 2, L 8192,
   Hq 64, Hkv 8, d 64, sink ~ N(0,1), dO ~ N(0,1).
+* ``extend_window``  -- the varlen extend with the first 1024 + last 7168 window
+  of sglang PR "To implement attention-sink" (Motivation and suggested code:
+  8192 visible tokens per query once a sequence is longer than that): 8
+  requests, prefix U{8192..32768} (so that the window skips keys), chunk
+  U{512..8192}, Hq 64, Hkv 8, d 64, sink ~ U(-2, 4).
 * ``extend_paged``   -- the ``extend_varlen`` shapes with each request's
   prefix in a paged cache (page 16, random page permutation; the serving
   extend path reads its prefix through the page table, sglang PR "To implement
@@ -333,6 +338,17 @@ def extend_varlen(seed=0, n_req=8):
                         seqlens_q=lens, hq=64, hkv=8, d=64, sink=(-2.0, 4.0), seed=seed)
 
 
+def extend_window(seed=0, n_req=8):
+    def lens(g):
+        prefix = _randint(g, 8192, 32768, n_req)
+        chunk = _randint(g, 512, 8192, n_req)
+        return chunk.tolist(), (prefix + chunk).tolist()
+    return make_prefill(name="extend_window 8req prefix U8192-32768 chunk U512-8192 Hq64 Hkv8 d64 sink "
+                             "first1024+last7168",
+                        seqlens_q=lens, hq=64, hkv=8, d=64, sink=(-2.0, 4.0), win_first=1024, win_last=7168,
+                        seed=seed)
+
+
 def decode_sink(seed=0):
     return make_decode(name="decode_sink B64 Hq64 Hkv8 d64 ps16 L U1024-32768 sink",
                        seqlens=lambda g: _randint(g, 1024, 32768, 64).tolist(),
@@ -367,6 +383,7 @@ def train(seed=0):
 WORKLOADS = {
     "prefill_tiny": prefill_tiny,
     "extend_varlen": extend_varlen,
+    "extend_window": extend_window,
     "decode_sink": decode_sink,
     "decode_window": decode_window,
     "train": train,

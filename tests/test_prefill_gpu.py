@@ -124,7 +124,7 @@ def _sample_rows(p, per_req, seed=0):
     return rows
 
 
-@pytest.mark.parametrize("name", ["prefill_tiny", "extend_varlen", "train"])
+@pytest.mark.parametrize("name", ["prefill_tiny", "extend_varlen", "extend_window", "train"])
 def test_full_size_workloads_sampled(ext, name):
     """The named workloads at full size in the bench's launch configuration;
     sampled rows (all heads) against the oracle, the tiny one completely."""

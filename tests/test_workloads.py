@@ -55,6 +55,20 @@ def test_extend_varlen_recipe(no_bulk):
     assert closed == 4_836_967_579_648  # the bench line's algorithmic TFLOP per step (seed 0)
 
 
+def test_extend_window_recipe(no_bulk):
+    p = wl.extend_window()
+    C = p.seqlens_q
+    P = [k - q for q, k in zip(p.seqlens_q, p.seqlens_k)]
+    assert len(C) == 8 and all(512 <= c <= 8192 for c in C) and all(8192 <= x <= 32768 for x in P)
+    assert (p.win_first, p.win_last) == (1024, 7168) and p.causal
+    # every query of a request sits at position >= 8191, so it sees exactly 1024 + 7168 keys
+    assert bench.fwd_flops(p) == 4 * 64 * 64 * 8192 * sum(C)
+    # and the visibility rule of the oracle agrees
+    for Lq, Lk in zip(C, p.seqlens_k):
+        (a0, b0), (a1, b1) = orc.visible_ranges(Lk - Lq + 1, 1024, 7168)
+        assert (b0 - a0) + (b1 - a1) == 8192
+
+
 def test_extend_paged_shares_the_lengths(no_bulk):
     p, pe = wl.extend_varlen(), wl.extend_paged()
     assert pe.seqlens_q == p.seqlens_q and pe.seqlens_k.tolist() == p.seqlens_k
