@@ -18,7 +18,7 @@
 //   warp 2      TMA producer of the V tiles (3-stage ring)
 // With a paged cache the producers fetch each tile as page segments through
 // the page table (one TMA copy per segment).
-//   warp 3      idle (completes warpgroup 0 for the register split)
+//   warp 3      tcgen05.mma issuer of O += P V (warp 1 then issues S only)
 //   warps 4..7  softmax warpgroup; thread = query row.
 // TMEM (256 columns): S at 0, O at 128, P (bf16 pairs) at 192.
 // The online softmax starts from m = sink, l = 1 (the sink costs nothing per
@@ -79,7 +79,7 @@ struct __align__(1024) Smem {
     uint64_t k_full[KSTAGE], k_empty[KSTAGE];
     uint64_t v_full[VSTAGE], v_empty[VSTAGE];
     uint64_t s_full, s_free, p_full, o_done;  // one phase per key tile
-    uint64_t final_bar;
+    uint64_t final_bar, final_pv;  // the S issuer's / the P V issuer's MMAs all complete
     uint64_t v_tail;  // the V tile that holds the request's last key lands here first
     uint32_t tmem_base;
     int abort;
@@ -194,6 +194,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         mbar_init(&S.p_full, 128);
         mbar_init(&S.o_done, 1);
         mbar_init(&S.final_bar, 1);
+        mbar_init(&S.final_pv, 1);
         mbar_init(&S.v_tail, 1);
         S.abort = 0;
         fence_mbar_init();
@@ -295,10 +296,14 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
             __syncwarp();
-        } else if (warp == 1 && ntiles > 0) {
-            // -------------------------------------------------------- MMA issuer
-            // The whole warp runs the loop converged (every lane waits;
-            // elect.sync picks the issuing lane).
+        } else if ((warp == 1 || warp == 3) && ntiles > 0) {
+            // -------------------------------------------------------- MMA issuers
+            // Warp 1 issues S = Q K^T, warp 3 O += P V: the tensor core gets two
+            // independent instruction streams, and the issue stalls of a blocked
+            // tcgen05.mma fall on two SM sub-partitions (warp w runs on
+            // sub-partition w % 4), each slowing one softmax warp, instead of one.
+            // Both warps run their loop converged (every lane waits; elect.sync
+            // picks the issuing lane).
             constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false, false);
             constexpr uint32_t idO = idesc_bf16_f32(BM, D, false, true);
             // Descriptor bases; a k-step adds its byte offset / 16 to the address field.
@@ -308,47 +313,45 @@ __global__ void __launch_bounds__(kThreads, 2)
             auto wait_all = [&](uint64_t* bar, uint32_t parity) {
                 return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
             };
-            auto issue_S = [&](int it) {
-                const uint64_t dk = dk0 + (it % KSTAGE) * (kTile >> 4);
-                // 16 head-dim elements = 32 bytes per k-step; atom kk / 4
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t o = (kk >> 2) * (kAtom >> 4) + (kk & 3) * 2;
-                    umma_ss_e(tmem + cS, dq + o, dk + o, idS, kk > 0);
-                }
-                umma_commit_e(&S.s_full);
-                umma_commit_e(&S.k_empty[it % KSTAGE]);
-            };
-            bool ok = wait_all(&S.q_full, 0) && wait_all(&S.k_full[0], 0);
-            if (ok) {
-                tc_fence_after();
-                issue_S(0);
-            }
-            for (int it = 0; ok && it < ntiles; ++it) {
-                const int nx = it + 1;
-                // The next S as soon as the softmax has read this one (it runs on
-                // the tensor core while the softmax works) ...
-                if (nx < ntiles) {
-                    if (!(ok = wait_all(&S.k_full[nx % KSTAGE], (nx / KSTAGE) & 1))) break;
-                    if (!(ok = wait_all(&S.s_free, it & 1))) break;
+            bool ok = true;
+            if (warp == 1) {
+                ok = wait_all(&S.q_full, 0);
+                for (int it = 0; ok && it < ntiles; ++it) {
+                    // S of tile it as soon as its K is in and the softmax has read the
+                    // previous S (it runs on the tensor core while the softmax works)
+                    if (!(ok = wait_all(&S.k_full[it % KSTAGE], (it / KSTAGE) & 1))) break;
+                    if (it > 0 && !(ok = wait_all(&S.s_free, (it - 1) & 1))) break;
                     tc_fence_after();
-                    issue_S(nx);
-                }
-                // ... then O += P V once P is in TMEM (8 columns of bf16 pairs per 16 keys;
-                // V rows 2048 bytes on per 16 keys).
-                if (!(ok = wait_all(&S.v_full[it % VSTAGE], (it / VSTAGE) & 1))) break;
-                if (!(ok = wait_all(&S.p_full, it & 1))) break;
-                tc_fence_after();
-                const uint64_t dv = dv0 + (it % VSTAGE) * (kTile >> 4);
+                    const uint64_t dk = dk0 + (it % KSTAGE) * (kTile >> 4);
+                    // 16 head-dim elements = 32 bytes per k-step; atom kk / 4
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    umma_ts_e(tmem + cO, tmem + cP + kk * 8, dv + 128 * kk, idO, (it > 0 || kk > 0) ? 1u : 0u);
-                umma_commit_e(&S.o_done);
-                umma_commit_e(&S.v_empty[it % VSTAGE]);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t o = (kk >> 2) * (kAtom >> 4) + (kk & 3) * 2;
+                        umma_ss_e(tmem + cS, dq + o, dk + o, idS, kk > 0);
+                    }
+                    umma_commit_e(&S.s_full);
+                    umma_commit_e(&S.k_empty[it % KSTAGE]);
+                }
+                // Every MMA issued must be complete before TMEM is released.
+                umma_commit_e(&S.final_bar);
+                drain_wait(&S.final_bar, 0);
+            } else {
+                for (int it = 0; ok && it < ntiles; ++it) {
+                    // O += P V once P is in TMEM (8 columns of bf16 pairs per 16 keys;
+                    // V rows 2048 bytes on per 16 keys)
+                    if (!(ok = wait_all(&S.v_full[it % VSTAGE], (it / VSTAGE) & 1))) break;
+                    if (!(ok = wait_all(&S.p_full, it & 1))) break;
+                    tc_fence_after();
+                    const uint64_t dv = dv0 + (it % VSTAGE) * (kTile >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        umma_ts_e(tmem + cO, tmem + cP + kk * 8, dv + 128 * kk, idO, (it > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit_e(&S.o_done);
+                    umma_commit_e(&S.v_empty[it % VSTAGE]);
+                }
+                umma_commit_e(&S.final_pv);
+                drain_wait(&S.final_pv, 0);
             }
-            // Every MMA issued must be complete before TMEM is released.
-            umma_commit_e(&S.final_bar);
-            drain_wait(&S.final_bar, 0);
         }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
