@@ -39,14 +39,18 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # Keyed by kernel + workload; each entry records the hash of the kernel source
 # it was measured on and is reported only while that source is unchanged.
 NCU_TRAFFIC = {
-    # fwd_kernel: 442.5 MB read + 258.5 MB written per launch
-    "fwd_kernel/extend_varlen": {"src": "aefeee9909ec7232", "bytes": 701_026_304},
-    # bwd_main_kernel: 2.594 GB read + 1.152 GB written per launch
-    "bwd_main_kernel/train": {"src": "42e25632af854dce", "bytes": 3_745_681_000},
-    # decode_split_kernel: 1.944 GB + 0.011 GB
-    "decode/decode_sink": {"src": "74c2b03b3cdc9cb0", "bytes": 1_954_192_080},
+    # fwd_kernel<64>: 442.5 MB read + 259.7 MB written per launch
+    "fwd_kernel/extend_varlen": {"src": "be9e0f6a91f4c9cf", "bytes": 702_200_576},
+    # fwd_kernel<64>, first 1024 + last 7168 window: 489.5 MB + 268.2 MB
+    "fwd_kernel/extend_window": {"src": "be9e0f6a91f4c9cf", "bytes": 757_656_320},
+    # fwd_kernel<64> reading K/V through a page-16 table: 448.7 MB + 259.3 MB
+    "fwd_kernel/extend_paged": {"src": "be9e0f6a91f4c9cf", "bytes": 707_991_552},
+    # bwd_main_kernel<64>: 2.428 GB read + 1.090 GB written per launch
+    "bwd_main_kernel/train": {"src": "5ff263e6c2749d8f", "bytes": 3_518_621_952},
+    # decode_split_kernel: 1.943 GB + 0.011 GB
+    "decode/decode_sink": {"src": "c0d40bc40087f07f", "bytes": 1_954_153_216},
     # decode_split_kernel: 1.074 GB + 0.007 GB
-    "decode/decode_window": {"src": "74c2b03b3cdc9cb0", "bytes": 1_080_889_760},
+    "decode/decode_window": {"src": "c0d40bc40087f07f", "bytes": 1_081_029_120},
 }
 
 
@@ -398,7 +402,8 @@ def bench_extend_paged(torch, ext, dev, pe, steps, warmup, flush, peaks, peak_sr
             "roofline": {"kernel": "attn_sink_fwd_paged call (kv_append_kernel + fwd_kernel, paged loads)",
                          "bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": tf / peaks["bf16_tflops"], "peak_source": f"bf16 burst, {peak_src}",
-                         "traffic": None, "algorithmic_flops_per_launch": flops}}
+                         "traffic": _traffic("fwd_kernel/extend_paged", "prefill_fwd.cu"),
+                         "algorithmic_flops_per_launch": flops}}
 
 
 def bench_decode_append(torch, ext, dev, dc, steps, warmup, flush, peaks, peak_src):
