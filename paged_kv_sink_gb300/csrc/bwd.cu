@@ -9,19 +9,26 @@
 //
 // Three kernels:
 //  * bwd_preprocess_kernel: D_i per (row, head) and dsink (warp shuffles, one
-//    fp32 atomic per block and head).
+//    fp32 atomic per block and head); it writes each row's -LSE / scale and -D
+//    as a 32-byte record of bf16 parts for the main kernel.
 //  * bwd_main_kernel (tcgen05): one CTA per (128-key tile, KV head, request);
 //    it loops over the query heads of the KV group and the 128-row query tiles
-//    that see its keys.  Per step five tcgen05 GEMMs:
-//        S = Q K^T, dP = dO V^T              (TMEM, 128 x 128 fp32 each)
-//        dV += P^T dO, dK += dS^T Q          (TMEM accumulators over the whole loop)
-//        dQ  = dS K                          (TMEM; A = dS read from TMEM)
-//    Two warpgroups share the elementwise work: thread = (query row, half of the
-//    128 key columns), so the row's LSE and D are per-thread scalars.  They
-//    write P and scale dS to shared memory in the 128-byte-swizzled layout (read
-//    MN-major as P^T / dS^T for dV / dK and K-major for dQ), and add the
-//    previous step's dQ tile to an fp32 accumulator with TMA bulk tensor
-//    reduce-adds.  dK/dV are summed over the group in TMEM (no atomics).
+//    that see its keys.  Per step five tcgen05 GEMMs, in the key-major
+//    orientation (a TMEM lane is a key):
+//        S^T = K Q^T, dP^T = V dO^T          (TMEM, 128 keys x 128 queries, fp32)
+//        dV += P^T dO, dK += dS^T Q          (A = P^T / dS^T read from TMEM;
+//                                             accumulated over the whole loop)
+//        dQ  = dS K                          (A = dS from shared memory)
+//    The per-query terms ride in the GEMMs: one more 16-wide k-step multiplies
+//    a block of ones (keys x 16) by the tile's 128 records (TMA-loaded with Q
+//    and dO), each holding -LSE / scale and -D of a query split into three bf16
+//    parts, so S^T comes out as S - LSE / scale and dP^T as dP - D.  Two warpgroups share
+//    the elementwise work: thread = (key, half of the 128 query columns), with
+//    no per-query data to fetch.  P^T and dS^T go to TMEM as bf16 pairs and dS
+//    to shared memory once (the MN-major A of dQ); the previous step's dQ tile
+//    is added to an fp32 accumulator with TMA bulk tensor reduce-adds.  dK / dV
+//    are summed over the group in TMEM (no atomics); dS leaves out the softmax
+//    scale, which dK and dQ take on their way out.
 //  * bwd_dq_convert_kernel: fp32 dQ accumulator -> bf16.
 #include <cudaTypedefs.h>
 
@@ -44,10 +51,10 @@ constexpr int kWork = 256;      // elementwise threads: warps 4..11
 constexpr uint32_t kTile = 128 * 128;  // one 128-byte-swizzled atom: 128 rows x 128 bytes
 // Head-dim dependent sizes.  A 128-row operand tile of Q, dO, K or V is D / 64
 // atoms (atom a: elements 64a .. 64a + 63 of every row, at byte offset
-// a * kTile).  At d 128 the products S and dP run over both atoms, and the main
-// kernel runs twice, each pass producing one 64-column half of dQ, dK and dV
-// (the TMEM budget -- S, dP, dV, dK, dQ and dS -- fits 64 output columns); the
-// Q / dO ring then has one stage to fit shared memory.
+// a * kTile).  At d 128 the products S^T and dP^T run over both atoms, and the
+// main kernel runs twice, each pass producing one 64-column half of dQ, dK and
+// dV (the TMEM budget fits 64 output columns); the Q / dO ring then has one
+// stage to fit shared memory.
 template <int D>
 struct Cfg {
     static constexpr int kAtoms = D / 64;
@@ -55,10 +62,20 @@ struct Cfg {
     static constexpr int kQStages = D == 64 ? 3 : 1;
 };
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: S, dP (fp32), dV, dK (fp32 accumulators over the whole loop),
-// dQ (fp32, one step) and dS (bf16 pairs: column c holds keys 2c and 2c+1), the
-// A operand of dQ = dS K read straight from TMEM.
-constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDK = 320, cDQ = 384, cDS = 448;
+// TMEM columns.  Lane = key for S^T, dP^T (fp32, column = query), dV, dK (fp32
+// accumulators over the whole loop) and P^T (bf16 pairs: column c holds queries
+// 2c and 2c + 1); lane = query for dQ (fp32, one step).  dS^T (bf16 pairs) is
+// written over the dP^T columns its thread has already read: the query half h
+// at cDP + 64 h, 32 columns.
+constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDK = 320, cDQ = 384, cPT = 448;
+// One 128-row K-major operand of a single k-step (16 bf16 = 32 bytes per row) in
+// the 32-byte-swizzled layout.
+constexpr uint32_t kAug = 128 * 32;
+// Per-query record (the B of the extra k-step): bf16 elements 0..2 hold
+// -LSE / scale as h1 + h2 + h3 (x - h1 and its remainder are exact in fp32; an
+// infinite value is stored as +-1e30), elements 8..10 hold -D the same way, the
+// rest are zero.
+constexpr int kRec = 16;
 
 template <int D>
 struct __align__(1024) Smem {
@@ -67,18 +84,25 @@ struct __align__(1024) Smem {
     uint8_t v[Cfg<D>::kOp];
     uint8_t q[kQStages][Cfg<D>::kOp];
     uint8_t dout[kQStages][Cfg<D>::kOp];
-    uint8_t pb[2 * kTile];   // P  (128 queries x 128 keys): two 64-key atoms of 128-byte rows
-    uint8_t dsb[2 * kTile];  // dS (same layout)
-    uint8_t dq_stage[2][kTile];  // dQ tile staging: two 32-column fp32 halves, 128-byte swizzled rows
+    uint8_t dsb[2 * kTile];       // dS: 128 key rows x 128 queries (two 64-query atoms), the MN-major A of dQ
+    uint8_t dq_stage[2][kTile];   // dQ tile staging: two 32-column fp32 halves, 128-byte swizzled rows
+    // The extra k-step of S^T and dP^T: A = ones_lse (1 in elements 0..2 of
+    // every key row) or ones_d (1 in elements 8..10), B = rec (the tile's
+    // per-query records).
+    uint8_t ones_lse[kAug];
+    uint8_t ones_d[kAug];
+    uint8_t rec[kQStages][kAug];
     uint64_t kv_full;
     uint64_t kv_ready;  // K / V rows past the request's last key zeroed (tail key tiles only)
     uint64_t qdo_tail;  // a head's last query tile reaching past the request lands here first
     uint64_t qdo_full[kQStages], qdo_empty[kQStages];
-    uint64_t sdp_full, sdp_free, pds_full, mma2_done;  // per step
+    uint64_t s_full, s_free, dp_full;           // per step: S^T read out, dP^T
+    uint64_t p_full;                            // P^T in TMEM (and the previous dQ read out)
+    uint64_t ds_full, mma2_done;                // dS^T / dS written; dK and dQ done
     uint64_t dq_staged;     // all elementwise threads wrote their part of the dQ tile
     uint64_t dq_stage_free; // the bulk reduce has finished reading the staging buffer
     uint64_t final_bar;  // dV / dK / dQ issuer done
-    uint64_t final_sdp;  // S / dP issuer done
+    uint64_t final_sdp;  // S^T / dP^T issuer done
     uint32_t tmem_base;
     int abort;
 };
@@ -86,8 +110,6 @@ struct __align__(1024) Smem {
 struct MainParams {
     const int32_t* cu_q;
     const int32_t* cu_k;
-    const float* lse;      // (hq, total_q)
-    const float* dvec;     // (hq, total_q)
     float* dq_accum;       // (total_q, hq, d) fp32
     __nv_bfloat16* dk;     // (total_k, hkv, d), rows dk_rs elements apart
     __nv_bfloat16* dv;     // rows dv_rs elements apart
@@ -134,29 +156,44 @@ __device__ __forceinline__ QRange query_tiles(int j0, int Lq, int Lk, int causal
     return r;
 }
 
-// P = 2^(S scale log2(e) - LSE log2(e)) and dS = P (dP - D) for 32 key columns of
-// one query row, packed to bf16 pairs; kMask zeroes the keys the row does not see
-// (c > c_last, or c_first_end <= c < c_win).
-template <bool kMask>
-__device__ __forceinline__ void p_ds_half(const uint32_t (&sr)[32], const uint32_t (&dr)[32], int col, uint64_t sc2,
-                                          uint64_t nl2x2, uint64_t scx2, uint64_t ndx2, int c_last, int c_first_end,
-                                          int c_win, uint32_t* pw, uint32_t* dw) {
+// P = 2^((S - LSE / scale) scale log2(e)) for the 32 query columns c0 .. c0 + 31
+// of one key (in place: pr holds the shifted S^T on entry, P in fp32 on exit)
+// and its bf16 pairs into pw[c0 / 2 ..]; kMask zeroes the columns e outside
+// [lo, hi] (a select: their shifted S may be anything).
+template <bool kMask, int c0>
+__device__ __forceinline__ void p_cols(uint32_t (&pr)[32], uint64_t sc2, int lo, int hi, uint32_t (&pw)[32]) {
 #pragma unroll
     for (int e = 0; e < 32; e += 2) {
-        const int c = col + e;
         float y0, y1;
-        f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sc2, nl2x2), y0, y1);
+        f2_unpack(f2_mul(f2_pack(__uint_as_float(pr[e]), __uint_as_float(pr[e + 1])), sc2), y0, y1);
         float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
         if (kMask) {
-            if (c > c_last || (c >= c_first_end && c < c_win)) p0 = 0.f;
-            if (c + 1 > c_last || (c + 1 >= c_first_end && c + 1 < c_win)) p1 = 0.f;
+            if (c0 + e < lo || c0 + e > hi) p0 = 0.f;
+            if (c0 + e + 1 < lo || c0 + e + 1 > hi) p1 = 0.f;
         }
-        const uint64_t ds = f2_mul(f2_pack(p0, p1),
-                                   f2_fma(f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), scx2, ndx2));
-        float d0, d1;
-        f2_unpack(ds, d0, d1);
-        pw[e >> 1] = pack_bf16x2(p0, p1);
-        dw[e >> 1] = pack_bf16x2(d0, d1);
+        pr[e] = __float_as_uint(p0);
+        pr[e + 1] = __float_as_uint(p1);
+        pw[(c0 + e) >> 1] = pack_bf16x2(p0, p1);
+    }
+}
+
+// dS / scale = P (dP - D) for the 32 query columns c0 .. c0 + 31 of one key (pr:
+// their P, dr: their shifted dP^T), as bf16 pairs into dw[c0 / 2 ..]; kMask
+// zeroes the columns e outside [lo, hi] (whose dP - D may be anything).
+template <bool kMask, int c0>
+__device__ __forceinline__ void ds_cols(const uint32_t (&pr)[32], const uint32_t (&dr)[32], int lo, int hi,
+                                        uint32_t (&dw)[32]) {
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+        float a0, a1;
+        f2_unpack(f2_mul(f2_pack(__uint_as_float(pr[e]), __uint_as_float(pr[e + 1])),
+                         f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1]))),
+                  a0, a1);
+        if (kMask) {
+            if (c0 + e < lo || c0 + e > hi) a0 = 0.f;
+            if (c0 + e + 1 < lo || c0 + e + 1 > hi) a1 = 0.f;
+        }
+        dw[(c0 + e) >> 1] = pack_bf16x2(a0, a1);
     }
 }
 
@@ -164,7 +201,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const __grid_constant__ CUtensorMap tm_dq, const MainParams p) {
+                    const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_rec,
+                    const MainParams p) {
     using C = Cfg<D>;
     constexpr int kQStages = C::kQStages;
     constexpr uint32_t kOp = C::kOp;
@@ -201,9 +239,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&S.qdo_full[s], 1);
             mbar_init(&S.qdo_empty[s], 1);
         }
-        mbar_init(&S.sdp_full, 1);
-        mbar_init(&S.sdp_free, kWork);
-        mbar_init(&S.pds_full, kWork);
+        mbar_init(&S.s_full, 1);
+        mbar_init(&S.s_free, kWork);
+        mbar_init(&S.dp_full, 1);
+        mbar_init(&S.p_full, kWork);
+        mbar_init(&S.ds_full, kWork);
         mbar_init(&S.mma2_done, 1);
         mbar_init(&S.dq_staged, kWork);
         mbar_init(&S.dq_stage_free, 1);
@@ -246,9 +286,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 prefetch_tmap(&tm_k);
                 prefetch_tmap(&tm_v);
                 prefetch_tmap(&tm_do);
+                prefetch_tmap(&tm_rec);
                 mbar_expect_tx(&S.kv_full, 2 * kOp);
                 tma_tile<D>(S.k, &tm_k, &S.kv_full, kvh, k_start + j0);
                 tma_tile<D>(S.v, &tm_v, &S.kv_full, kvh, k_start + j0);
+            }
+            {
+                // The two ones blocks.  Row j is 32 bytes at j * 32; the 32-byte
+                // swizzle stores its 16-byte half c at half c ^ (bit 2 of j).  They
+                // are read only by MMAs that wait on a barrier this warp's lane 0
+                // arrives on after the fence below.
+                const uint4 one = make_uint4(0x3F803F80u, 0x00003F80u, 0u, 0u);  // bf16 1, 1, 1, 0 ...
+                const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+                for (int c = lane; c < (int)(kAug / 16); c += 32) {
+                    const int j = c >> 1, half = (c & 1) ^ ((j >> 2) & 1);  // logical half stored here
+                    reinterpret_cast<uint4*>(S.ones_lse)[c] = half == 0 ? one : zero;
+                    reinterpret_cast<uint4*>(S.ones_d)[c] = half == 1 ? one : zero;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
             }
             bool ok = true;
             if (kv_tail) {
@@ -263,6 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             int t = 0, g_c = 0, qt_c = 0, tails = 0;
             bool tail_pending = false;
+            uint32_t tail_last = 0;  // bit st: the last load into stage st went through qdo_tail
             for (; ok && t < T; ++t) {
                 const int st = t % kQStages;
                 if (t >= kQStages &&
@@ -273,10 +330,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool tail = q0 + BM > Lq;
                 uint64_t* bar = tail ? &S.qdo_tail : &S.qdo_full[st];
                 if (lane == 0) {
-                    mbar_expect_tx(bar, 2 * kOp);
+                    mbar_expect_tx(bar, 2 * kOp + kAug);
                     tma_tile<D>(S.q[st], &tm_q, bar, h, q_start + q0);
                     tma_tile<D>(S.dout[st], &tm_do, bar, h, q_start + q0);
+                    tma_load_3d(S.rec[st], &tm_rec, bar, 0, h, q_start + q0);
                 }
+                tail_last = tail ? (tail_last | (1u << st)) : (tail_last & ~(1u << st));
                 if (tail) {
                     tail_pending = true;
                     if (!__all_sync(0xffffffffu, mbar_wait(&S.qdo_tail, tails & 1, abort))) break;
@@ -294,11 +353,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (lane == 0) {
+                // the copies in flight land before the CTA exits
                 drain_wait(&S.kv_full, 0);
                 if (tail_pending) drain_wait(&S.qdo_tail, tails & 1);
                 for (int st = 0; st < kQStages; ++st) {
                     const int n = t > st ? (t - st + kQStages - 1) / kQStages : 0;  // loads issued into stage st
-                    if (n > 0) drain_wait(&S.qdo_full[st], (n - 1) & 1);
+                    if (n > 0 && !((tail_last >> st) & 1u)) drain_wait(&S.qdo_full[st], (n - 1) & 1);
                 }
             }
             __syncwarp();
@@ -330,22 +390,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if ((warp == 1 || warp == 3) && T > 0) {
             // -------------------------------------------------------- MMA issuers
             // Two issuing warps feed the tensor core independent instruction
-            // streams: warp 1 issues each step's S / dP as soon as the
-            // elementwise warps have read the previous ones; warp 3 issues the
-            // step's dV / dK / dQ once P and dS are in shared memory.  Both run
-            // converged (every lane waits; elect.sync picks the issuing lane),
-            // and within a stream the independent accumulator chains are
-            // interleaved k-step by k-step.
-            constexpr uint32_t idSS = idesc_bf16_f32(BM, BN, false, false);  // S, dP: both K-major
-            constexpr uint32_t idKV = idesc_bf16_f32(BN, DH, true, true);    // dV, dK: A (P^T, dS^T) MN-major
-            constexpr uint32_t idQ = idesc_bf16_f32(BM, DH, false, true);    // dQ: A (dS) K-major, B (K) MN-major
+            // streams: warp 1 issues each step's S^T as soon as the elementwise
+            // warps have read the previous one, and dP^T once dK has read the
+            // previous dS^T (which sits in the dP^T columns); warp 3 issues dV
+            // once P^T is in TMEM, then dK / dQ once dS^T / dS are written.  Both
+            // run converged (every lane waits; elect.sync picks the issuing lane),
+            // and dK / dQ are interleaved k-step by k-step.
+            constexpr uint32_t idSS = idesc_bf16_f32(BN, BM, false, false);  // S^T, dP^T: both K-major
+            constexpr uint32_t idKV = idesc_bf16_f32(BN, DH, false, true);   // dV, dK: A in TMEM, B (dO, Q) MN-major
+            constexpr uint32_t idQ = idesc_bf16_f32(BM, DH, true, true);     // dQ: A (dS) and B (K) MN-major
             const uint32_t half_off = (uint32_t)p.dhalf * (kTile >> 4);      // this pass's 64-column atom
             // Descriptor bases; a k-step adds its byte offset / 16 to the address field.
-            const uint64_t dk_k = sdesc_sw128(smem_u32(S.k), 16, 1024);        // K, K-major (B of S)
-            const uint64_t dv_k = sdesc_sw128(smem_u32(S.v), 16, 1024);        // V, K-major (B of dP)
+            const uint64_t dk_k = sdesc_sw128(smem_u32(S.k), 16, 1024);        // K, K-major (A of S^T)
+            const uint64_t dv_k = sdesc_sw128(smem_u32(S.v), 16, 1024);        // V, K-major (A of dP^T)
+            const uint64_t d_ones_lse = sdesc_sw32(smem_u32(S.ones_lse));      // A of the extra k-step of S^T
+            const uint64_t d_ones_d = sdesc_sw32(smem_u32(S.ones_d));          // ... and of dP^T
             const uint64_t dk_mn = sdesc_sw128(smem_u32(S.k), 8192, 1024) + half_off;  // K, MN-major (B of dQ)
-            const uint64_t dp_mn = sdesc_sw128(smem_u32(S.pb), kTile, 1024);   // P^T, MN-major (A of dV)
-            const uint64_t ds_mn = sdesc_sw128(smem_u32(S.dsb), kTile, 1024);  // dS^T, MN-major (A of dK)
+            const uint64_t ds_mn = sdesc_sw128(smem_u32(S.dsb), kTile, 1024);  // dS, MN-major (A of dQ)
             auto wait_all = [&](uint64_t* bar, uint32_t parity) {
                 return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
             };
@@ -354,17 +415,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int t = 0; ok && t < T; ++t) {
                     const int st = t % kQStages;
                     if (!(ok = wait_all(&S.qdo_full[st], (t / kQStages) & 1))) break;
-                    if (t > 0 && !(ok = wait_all(&S.sdp_free, (t - 1) & 1))) break;
+                    if (t > 0 && !(ok = wait_all(&S.s_free, (t - 1) & 1))) break;
                     tc_fence_after();
                     const uint64_t dq_k = sdesc_sw128(smem_u32(S.q[st]), 16, 1024);
                     const uint64_t ddo_k = sdesc_sw128(smem_u32(S.dout[st]), 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {  // 16 head-dim elements = 32 bytes per k-step
                         const uint32_t o = (kk >> 2) * (kTile >> 4) + (kk & 3) * 2;  // atom kk / 4
-                        umma_ss_e(tmem + cS, dq_k + o, dk_k + o, idSS, kk > 0);
-                        umma_ss_e(tmem + cDP, ddo_k + o, dv_k + o, idSS, kk > 0);
+                        umma_ss_e(tmem + cS, dk_k + o, dq_k + o, idSS, kk > 0);
                     }
-                    umma_commit_e(&S.sdp_full);
+                    umma_ss_e(tmem + cS, d_ones_lse, sdesc_sw32(smem_u32(S.rec[st])), idSS, 1u);  // - LSE / scale
+                    umma_commit_e(&S.s_full);
+                    if (t > 0 && !(ok = wait_all(&S.mma2_done, (t - 1) & 1))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t o = (kk >> 2) * (kTile >> 4) + (kk & 3) * 2;
+                        umma_ss_e(tmem + cDP, dv_k + o, ddo_k + o, idSS, kk > 0);
+                    }
+                    umma_ss_e(tmem + cDP, d_ones_d, sdesc_sw32(smem_u32(S.rec[st])), idSS, 1u);  // - D
+                    umma_commit_e(&S.dp_full);
                 }
                 // Every MMA this warp issued must be complete before TMEM is released.
                 umma_commit_e(&S.final_sdp);
@@ -372,21 +442,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 for (int t = 0; ok && t < T; ++t) {
                     const int st = t % kQStages;
-                    // pds_full also means the previous dQ has been read out of TMEM
-                    if (!(ok = wait_all(&S.pds_full, t & 1))) break;
+                    if (!(ok = wait_all(&S.p_full, t & 1))) break;
+                    tc_fence_after();
+                    const uint64_t ddo_mn = sdesc_sw128(smem_u32(S.dout[st]), 8192, 1024) + half_off;
+                    // dV: k-step kk runs over queries 16 kk .. 16 kk + 15 (P^T: 8 TMEM
+                    // columns per step; MN-major dO: 2048 bytes per step)
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        umma_ts_e(tmem + cDV, tmem + cPT + kk * 8, ddo_mn + 128 * kk, idKV, (t > 0 || kk > 0) ? 1u : 0u);
+                    // dS^T / dS written
+                    if (!(ok = wait_all(&S.ds_full, t & 1))) break;
                     tc_fence_after();
                     const uint64_t dq_mn = sdesc_sw128(smem_u32(S.q[st]), 8192, 1024) + half_off;
-                    const uint64_t ddo_mn = sdesc_sw128(smem_u32(S.dout[st]), 8192, 1024) + half_off;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        // dV / dK: k-step kk runs over query rows 16 kk .. 16 kk + 15 of P / dS
-                        // (2048 bytes into the MN-major A and B alike)
-                        const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
-                        umma_ss_e(tmem + cDV, dp_mn + 128 * kk, ddo_mn + 128 * kk, idKV, acc);
-                        umma_ss_e(tmem + cDK, ds_mn + 128 * kk, dq_mn + 128 * kk, idKV, acc);
-                        // dQ: k-step kk runs over keys 16 kk .. 16 kk + 15 (dS in TMEM: 8 columns
-                        // per step; MN-major K: 2048 bytes per step)
-                        umma_ts_e(tmem + cDQ, tmem + cDS + kk * 8, dk_mn + 128 * kk, idQ, kk > 0);
+                        // dK: queries 16 kk .. 16 kk + 15; dS^T of query half kk / 4 sits at
+                        // cDP + 64 (kk / 4), 8 columns per step
+                        const uint32_t a_ds = tmem + cDP + 64 * (kk >> 2) + 8 * (kk & 3);
+                        umma_ts_e(tmem + cDK, a_ds, dq_mn + 128 * kk, idKV, (t > 0 || kk > 0) ? 1u : 0u);
+                        // dQ: keys 16 kk .. 16 kk + 15 (2048 bytes into the MN-major dS and K alike)
+                        umma_ss_e(tmem + cDQ, ds_mn + 128 * kk, dk_mn + 128 * kk, idQ, kk > 0);
                     }
                     umma_commit_e(&S.mma2_done);
                     umma_commit_e(&S.qdo_empty[st]);
@@ -398,131 +473,103 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsWork));
         // ------------------------------------------------------------ elementwise
-        // Lane = query row i of the tile (TMEM lanes of S, dP and dQ) and key row
-        // i of the CTA (TMEM lanes of dK, dV); column half ch = keys [64 ch, 64 ch + 64).
+        // Lane = key r of the CTA (TMEM lane of S^T, dP^T, P^T, dS^T, dV, dK) and
+        // query row r of the tile (TMEM lane of dQ); hh = query half: columns
+        // 64 hh .. 64 hh + 63 of S^T / dP^T, dQ columns 32 hh .. 32 hh + 31.
         const int q4 = warp & 3;
-        const int ch = (warp - 4) >> 2;
-        const int i = q4 * 32 + lane;
+        const int hh = (warp - 4) >> 2;
+        const int r = q4 * 32 + lane;
         const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
         const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
-        const uint64_t scx2 = f2_pack(p.scale, p.scale);
         const int F = p.win_first, W = p.win_last;
+        const int kpos = j0 + r;
         bool ok = true;
 
         // The dQ tile of step tt (its GEMMs complete) leaves through shared memory:
-        // this lane's query row, 32 columns (half ch), is loaded from TMEM while the
-        // step's P / dS are stored, then staged; warp 2 adds the staged tile to the
-        // fp32 accumulator with TMA bulk reduce-adds.  dS carries the softmax scale,
-        // so the values go out as they are.
-        uint32_t* const stage_row = reinterpret_cast<uint32_t*>(S.dq_stage[ch] + i * 128);
+        // this lane's query row, 32 columns (half hh), is loaded from TMEM while the
+        // step's dS is stored, then staged times the softmax scale (dS leaves it
+        // out); warp 2 adds the staged tile to the fp32 accumulator with TMA bulk
+        // reduce-adds.
+        uint32_t* const stage_row = reinterpret_cast<uint32_t*>(S.dq_stage[hh] + r * 128);
         // Query rows past the request's end (another request's rows) are staged as
         // zeros: their dS is zero, but times a non-finite key it would not be.
+        const uint64_t scx2 = f2_pack(p.scale, p.scale);
         auto stage_dq = [&](uint32_t (&u)[32], int q0_row) {
-            if (q0_row + i >= Lq) {
+            const bool valid = q0_row + r < Lq;
 #pragma unroll
-                for (int c = 0; c < 32; ++c) u[c] = 0u;
+            for (int c = 0; c < 32; c += 2) {
+                float a, b;
+                f2_unpack(f2_mul(f2_pack(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), scx2), a, b);
+                u[c] = valid ? __float_as_uint(a) : 0u;
+                u[c + 1] = valid ? __float_as_uint(b) : 0u;
             }
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(smem_u32(stage_row) + (((c ^ (i & 7))) << 4)),
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(smem_u32(stage_row) + (((c ^ (r & 7))) << 4)),
                              "r"(u[4 * c]), "r"(u[4 * c + 1]), "r"(u[4 * c + 2]), "r"(u[4 * c + 3])
                              : "memory");
-            }
-        };
-        // LSE and D of this lane's query row for head g of the group and query tile
-        // qt (+inf / 0 past the request's end and past the last step)
-        auto load_row = [&](int g, int qt, float& lse, float& dd) {
-            const int row = (qr.lo + qt) * BM + i;
-            lse = INFINITY;
-            dd = 0.f;
-            if (g < p.group && row < Lq) {
-                const size_t at = (size_t)(kvh * p.group + g) * p.total_q + q_start + row;
-                lse = __ldg(p.lse + at);
-                dd = __ldg(p.dvec + at);
             }
         };
 
         // step t = g_c * nqt + qt_c (head g_c of the group, query tile qt_c)
         int g_c = 0, qt_c = 0;
         int q0_prev = 0;  // first query row of the previous step's tile
-        float lse_cur, d_cur;
-        load_row(0, 0, lse_cur, d_cur);
         for (int t = 0; t < T; ++t) {
             const int q0 = (qr.lo + qt_c) * BM;
-            int g_n = g_c, qt_n = qt_c + 1;
-            if (qt_n == nqt) {
-                qt_n = 0;
-                ++g_n;
-            }
-            float lse_nxt, d_nxt;
-            load_row(g_n, qt_n, lse_nxt, d_nxt);  // in flight while this step computes
-            ok = mbar_wait(&S.sdp_full, t & 1, abort);
+            ok = mbar_wait(&S.s_full, t & 1, abort);
             if (!__all_sync(0xffffffffu, ok)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const int rows_valid = min(BM, Lq - q0);
-            const int P0 = off + q0, P1 = off + q0 + rows_valid - 1;
-            const int jmax = j0 + BN - 1;
-            const bool full = (!p.causal || jmax <= P0) && (jmax < Lk) &&
-                              (W <= 0 || jmax < F || j0 >= P1 + 1 - W);
-            // visible key columns of this query: c <= c_last and (c < c_first_end or c >= c_win)
-            const int qpos = off + q0 + i;
-            const int c_last = min(Lk - 1, p.causal ? qpos : Lk - 1) - j0;
-            const int c_first_end = W > 0 ? F - j0 : BN;
-            const int c_win = W > 0 ? qpos + 1 - W - j0 : 0;
-            const float nl2 = -lse_cur * ATTN_LOG2E;  // -inf past the end: P = 0 there
-            const uint64_t nl2x2 = f2_pack(nl2, nl2);
-            const uint64_t ndx2 = f2_pack(-d_cur * p.scale, -d_cur * p.scale);
-            uint32_t pw[32], dw[32];  // packed bf16 P and dS of this query row, 64 key columns
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t sr[32], dr[32];
-                const uint32_t col = ch * 64 + half * 32;
-                tmem_ld32(tmem + lane_base + cS + col, sr);
-                tmem_ld32(tmem + lane_base + cDP + col, dr);
-                tmem_ld_wait();
-                if (half == 1) {  // S / dP fully read: the next step may overwrite them
-                    tc_fence_before();
-                    mbar_arrive(&S.sdp_free);
-                }
-                if (full)
-                    p_ds_half<false>(sr, dr, col, sc2, nl2x2, scx2, ndx2, c_last, c_first_end, c_win,
-                                     pw + half * 16, dw + half * 16);
-                else
-                    p_ds_half<true>(sr, dr, col, sc2, nl2x2, scx2, ndx2, c_last, c_first_end, c_win,
-                                    pw + half * 16, dw + half * 16);
+            uint32_t pa[32], pb[32];  // S^T, then P (fp32), of this key's queries 0..31 / 32..63 of the half
+            tmem_ld32(tmem + lane_base + cS + 64 * hh, pa);
+            tmem_ld32(tmem + lane_base + cS + 64 * hh + 32, pb);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(&S.s_free);
+            // Columns e (queries q0 + 64 hh + e) that see this key: lo <= e <= hi.
+            // Query position pos sees key kpos iff kpos < Lk, kpos <= pos (causal)
+            // and (kpos < F or kpos >= pos + 1 - W) (window); the columns past the
+            // request's last query (another request's records) are out too.
+            const long long base = (long long)off + q0 + 64 * hh;  // position of column 0
+            int lo = 0;
+            long long hi_ll = (long long)Lq - 1 - q0 - 64 * hh;
+            if (kpos >= Lk) {
+                lo = 64;
+            } else {
+                if (p.causal) lo = (int)max(0LL, min(64LL, (long long)kpos - base));
+                if (W > 0 && kpos >= F) hi_ll = min(hi_ll, (long long)kpos + W - 1 - base);
             }
-            uint32_t u[32];  // dQ of step t - 1
-            if (t > 0) {  // the previous step's GEMMs must be done reading P / dS
+            const int hi = (int)max(-1LL, min(63LL, hi_ll));
+            const bool full = __all_sync(0xffffffffu, lo == 0 && hi == 63);
+            uint32_t pw[32];
+            if (full) {
+                p_cols<false, 0>(pa, sc2, lo, hi, pw);
+                p_cols<false, 32>(pb, sc2, lo, hi, pw);
+            } else {
+                p_cols<true, 0>(pa, sc2, lo, hi, pw);
+                p_cols<true, 32>(pb, sc2, lo, hi, pw);
+            }
+            if (t > 0) {
+                // dV, dK and dQ of the previous step are done: P^T, dS^T (in the dP^T
+                // columns, which dP^T of this step overwrote after that) and dS are
+                // free again, and dQ of the previous step is ready
                 ok = mbar_wait(&S.mma2_done, (t - 1) & 1, abort);
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                tmem_ld32(tmem + lane_base + cDQ + ch * 32, u);
             }
-            // dS of this row's 64 keys into TMEM for dQ = dS K
-            tmem_st32(tmem + lane_base + cDS + ch * 32, *reinterpret_cast<uint32_t(*)[32]>(&dw[0]));
-            // 64 key columns = atom ch, chunks 0..7 of 16 bytes
-#pragma unroll
-            for (int cc = 0; cc < 8; ++cc) {
-                const uint32_t o = ch * kTile + sw128_off(i, cc);
-                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(smem_u32(S.pb + o)), "r"(pw[4 * cc]),
-                             "r"(pw[4 * cc + 1]), "r"(pw[4 * cc + 2]), "r"(pw[4 * cc + 3])
-                             : "memory");
-                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(smem_u32(S.dsb + o)), "r"(dw[4 * cc]),
-                             "r"(dw[4 * cc + 1]), "r"(dw[4 * cc + 2]), "r"(dw[4 * cc + 3])
-                             : "memory");
-            }
-            fence_proxy_async_smem();
-            tmem_st_wait();
-            if (t > 0) tmem_ld_wait();  // dQ of step t - 1 is out of TMEM before the next dQ GEMM
-            tc_fence_before();
-            mbar_arrive(&S.pds_full);
+            tmem_st32(tmem + lane_base + cPT + 32 * hh, pw);
             if (t > 0) {
+                uint32_t u[32];  // dQ of step t - 1, out of TMEM before this step's dQ GEMM
+                tmem_ld32(tmem + lane_base + cDQ + hh * 32, u);
+                tmem_ld_wait();
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&S.p_full);
                 // the bulk reduce of step t - 2 has finished reading the stage
                 ok = t == 1 || mbar_wait(&S.dq_stage_free, (t - 2) & 1, abort);
                 if (!__all_sync(0xffffffffu, ok)) {
@@ -532,20 +579,60 @@ __global__ void __launch_bounds__(kThreads, 1)
                 stage_dq(u, q0_prev);
                 fence_proxy_async_smem();
                 mbar_arrive(&S.dq_staged);
+            } else {
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&S.p_full);
             }
+            ok = mbar_wait(&S.dp_full, t & 1, abort);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t dw[32];  // dS / scale of this key's 64 queries, bf16 pairs
+            {
+                uint32_t dr[32];
+                tmem_ld32(tmem + lane_base + cDP + 64 * hh, dr);
+                tmem_ld_wait();
+                if (full)
+                    ds_cols<false, 0>(pa, dr, lo, hi, dw);
+                else
+                    ds_cols<true, 0>(pa, dr, lo, hi, dw);
+                tmem_ld32(tmem + lane_base + cDP + 64 * hh + 32, dr);
+                tmem_ld_wait();
+                if (full)
+                    ds_cols<false, 32>(pb, dr, lo, hi, dw);
+                else
+                    ds_cols<true, 32>(pb, dr, lo, hi, dw);
+            }
+            // dS^T into this thread's dP^T columns (read above): the A of dK
+            tmem_st32(tmem + lane_base + cDP + 64 * hh, dw);
+            // dS row r (64 queries = atom hh, chunks 0..7 of 16 bytes): the A of dQ
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {
+                const uint32_t o = hh * kTile + sw128_off(r, cc);
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(smem_u32(S.dsb + o)), "r"(dw[4 * cc]),
+                             "r"(dw[4 * cc + 1]), "r"(dw[4 * cc + 2]), "r"(dw[4 * cc + 3])
+                             : "memory");
+            }
+            fence_proxy_async_smem();
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&S.ds_full);
             q0_prev = q0;
-            lse_cur = lse_nxt;
-            d_cur = d_nxt;
-            g_c = g_n;
-            qt_c = qt_n;
+            if (++qt_c == nqt) {
+                qt_c = 0;
+                ++g_c;
+            }
         }
-        // last step's dQ, then dK (column half 0) / dV (column half 1)
+        // last step's dQ, then dK (query half 0) / dV (query half 1)
         if (ok && T > 0) {
             ok = __all_sync(0xffffffffu, mbar_wait(&S.mma2_done, (T - 1) & 1, abort));
             if (ok) {
                 tc_fence_after();
                 uint32_t u[32];
-                tmem_ld32(tmem + lane_base + cDQ + ch * 32, u);
+                tmem_ld32(tmem + lane_base + cDQ + hh * 32, u);
                 tmem_ld_wait();
                 ok = __all_sync(0xffffffffu, T == 1 || mbar_wait(&S.dq_stage_free, (T - 2) & 1, abort));
                 if (ok) {
@@ -559,12 +646,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xffffffffu, ok);
         const bool have = ok && T > 0;
         if (have) tc_fence_after();
-        const int kpos = j0 + i;
         const size_t rowoff =
-            (size_t)(k_start + kpos) * (size_t)(ch == 0 ? p.dk_rs : p.dv_rs) + (size_t)kvh * D + p.dhalf * DH;
-        const uint32_t col = ch == 0 ? cDK : cDV;
-        const float f = 1.f;  // dK: the scale rides on dS
-        __nv_bfloat16* outp = ch == 0 ? p.dk : p.dv;
+            (size_t)(k_start + kpos) * (size_t)(hh == 0 ? p.dk_rs : p.dv_rs) + (size_t)kvh * D + p.dhalf * DH;
+        const uint32_t col = hh == 0 ? cDK : cDV;
+        __nv_bfloat16* outp = hh == 0 ? p.dk : p.dv;
+        const float f = hh == 0 ? p.scale : 1.f;  // dK takes the softmax scale that dS left out
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             uint32_t u[32];
@@ -599,19 +685,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// D_i = rowsum(dO_i o O_i) and dsink.  Block: 256 threads, 64 rows of one head;
-// 8 threads per row, 16 bytes each.
+// D_i = rowsum(dO_i o O_i), the per-query records and dsink.  Block: 256
+// threads, 64 rows of one head; 8 threads per row, 16 bytes each.
+
+// x as three bf16 (h1 = x rounded, h2 = the remainder rounded, h3 = what is left
+// rounded: x - h1 and x - h1 - h2 are exact in fp32), elements 0..2 of a 16-byte
+// half-record.  An infinite x is stored as +-1e30: the k-step multiplies the
+// other half of the record by zeros, and 0 times an infinity would be NaN;
+// +-1e30 still drives P to 0 (or the column is masked anyway).
+__device__ __forceinline__ uint4 split3_bf16(float x) {
+    if (isinf(x)) x = copysignf(1e30f, x);
+    const float h1 = __bfloat162float(__float2bfloat16_rn(x));
+    float r = x - h1;
+    const float h2 = __bfloat162float(__float2bfloat16_rn(r));
+    r -= h2;
+    return make_uint4(pack_bf16x2(h1, h2), pack_bf16x2(r, 0.f), 0u, 0u);
+}
 
 template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ out,
                                                              const __nv_bfloat16* __restrict__ dout,
                                                              const float* __restrict__ lse,
-                                                             const float* __restrict__ sink, float* __restrict__ dvec,
+                                                             const float* __restrict__ sink, uint4* __restrict__ rec,
                                                              float* __restrict__ dsink, int total_q, int hq,
-                                                             const int32_t* __restrict__ cu_q, int batch) {
+                                                             float scale, const int32_t* __restrict__ cu_q,
+                                                             int batch) {
     const int h = blockIdx.y;
     // Rows past the last request (cu_q[batch] <= row < total_q) belong to no
-    // request: D = 0 and no sink term, whatever the buffers hold there.
+    // request: D = 0, a zero record and no sink term, whatever the buffers hold
+    // there.
     const int rows = min(total_q, max(0, cu_q[batch]));
     const int tid = threadIdx.x;
     const int sub = tid & 7;
@@ -635,10 +737,11 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
         d += __shfl_xor_sync(0xffffffffu, d, 1);
         d += __shfl_xor_sync(0xffffffffu, d, 2);
         d += __shfl_xor_sync(0xffffffffu, d, 4);
-        if (row < total_q && sub == 0) {
-            dvec[(size_t)h * total_q + row] = d;
-            if (sink && row < rows) {
-                const float l = lse[(size_t)h * total_q + row];
+        if (row < total_q && sub < 2) {
+            // record (row, h): two 16-byte halves, -LSE / scale (sub 0) and -D (sub 1)
+            const float l = (sub == 0 && row < rows) ? lse[(size_t)h * total_q + row] : 0.f;
+            rec[((size_t)row * hq + h) * 2 + sub] = split3_bf16(sub == 0 ? -l / scale : -d);
+            if (sub == 0 && sink && row < rows) {
                 // probability mass on the sink, e^{sink - LSE}
                 float ps;
                 if (sg == -INFINITY)
@@ -679,11 +782,13 @@ __global__ void bwd_dq_convert_kernel(const float4* __restrict__ acc, uint2* __r
 cudaError_t make_map(CUtensorMap* m, const void* base, int d, int heads, long long rows, std::string* what,
                      long long row_stride = 0);
 cudaError_t make_map_dq(CUtensorMap* m, const float* base, int d, int heads, long long rows, std::string* what);
+cudaError_t make_map_rec(CUtensorMap* m, const void* base, int heads, long long rows, std::string* what);
 
+// The fp32 dQ accumulator, then the per-query records (32 bytes per row and head).
 size_t workspace_bytes(const Args& a) {
     const size_t acc = (size_t)a.total_q * a.hq * a.head_dim * sizeof(float);
-    const size_t dv = (size_t)a.hq * a.total_q * sizeof(float);
-    return ((acc + 255) & ~size_t(255)) + dv;
+    const size_t rec = (size_t)a.total_q * a.hq * kRec * 2;
+    return ((acc + 255) & ~size_t(255)) + rec;
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -743,12 +848,34 @@ cudaError_t make_map_dq(CUtensorMap* m, const float* base, int D, int heads, lon
     return cudaSuccess;
 }
 
+// (rows, heads, 16) bf16 per-query records as {16, head, row}; box {16, 1, 128},
+// 32-byte swizzle (the layout of the extra k-step's B operand).
+cudaError_t make_map_rec(CUtensorMap* m, const void* base, int heads, long long rows, std::string* what) {
+    auto fn = encode_fn();
+    if (!fn) {
+        *what = "cuTensorMapEncodeTiled unavailable";
+        return cudaErrorNotSupported;
+    }
+    cuuint64_t dims[3] = {(cuuint64_t)kRec, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1)};
+    cuuint64_t strides[2] = {(cuuint64_t)kRec * 2, (cuuint64_t)kRec * 2 * heads};
+    cuuint32_t box[3] = {(cuuint32_t)kRec, 1, 128};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        *what = "cuTensorMapEncodeTiled (records) failed (" + std::to_string((int)r) + ")";
+        return cudaErrorInvalidValue;
+    }
+    return cudaSuccess;
+}
+
 template <int D>
 static cudaError_t launch_d(const Args& a, void* workspace, cudaStream_t s, std::string* what) {
     cudaError_t e;
     const size_t acc_bytes = (size_t)a.total_q * a.hq * D * sizeof(float);
     float* dq_accum = static_cast<float*>(workspace);
-    float* dvec = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((acc_bytes + 255) & ~size_t(255)));
+    uint4* rec = reinterpret_cast<uint4*>(static_cast<char*>(workspace) + ((acc_bytes + 255) & ~size_t(255)));
     if (a.dsink && (e = cudaMemsetAsync(a.dsink, 0, sizeof(float) * a.hq, s)) != cudaSuccess) {
         *what = "memset dsink";
         return e;
@@ -769,24 +896,23 @@ static cudaError_t launch_d(const Args& a, void* workspace, cudaStream_t s, std:
         dim3 g1((a.total_q + 63) / 64, a.hq);
         bwd_preprocess_kernel<D><<<g1, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(a.out),
                                                  reinterpret_cast<const __nv_bfloat16*>(a.dout), a.lse, a.sink,
-                                                 dvec, a.dsink, a.total_q, a.hq, a.cu_q, a.batch);
+                                                 rec, a.dsink, a.total_q, a.hq, a.scale, a.cu_q, a.batch);
         if ((e = cudaGetLastError()) != cudaSuccess) {
             *what = "preprocess launch";
             return e;
         }
     }
     if (a.total_q > 0 && a.total_k > 0 && a.max_seqlen_k > 0) {
-        CUtensorMap tq, tk, tv, tdo, tdq;
+        CUtensorMap tq, tk, tv, tdo, tdq, trec;
         if ((e = make_map(&tq, a.q, D, a.hq, a.total_q, what, a.q_rs)) != cudaSuccess) return e;
         if ((e = make_map(&tk, a.k, D, a.hkv, a.total_k, what, a.k_rs)) != cudaSuccess) return e;
         if ((e = make_map(&tv, a.v, D, a.hkv, a.total_k, what, a.v_rs)) != cudaSuccess) return e;
         if ((e = make_map(&tdo, a.dout, D, a.hq, a.total_q, what)) != cudaSuccess) return e;
         if ((e = make_map_dq(&tdq, dq_accum, D, a.hq, a.total_q, what)) != cudaSuccess) return e;
+        if ((e = make_map_rec(&trec, rec, a.hq, a.total_q, what)) != cudaSuccess) return e;
         MainParams p;
         p.cu_q = a.cu_q;
         p.cu_k = a.cu_k;
-        p.lse = a.lse;
-        p.dvec = dvec;
         p.dq_accum = dq_accum;
         p.dk = reinterpret_cast<__nv_bfloat16*>(a.dk);
         p.dv = reinterpret_cast<__nv_bfloat16*>(a.dv);
@@ -803,6 +929,7 @@ static cudaError_t launch_d(const Args& a, void* workspace, cudaStream_t s, std:
         p.scale = a.scale;
         p.scale_log2 = a.scale * ATTN_LOG2E;
         const size_t smem = sizeof(Smem<D>) + 1024;
+        static_assert(sizeof(Smem<D>) + 1024 <= 227 * 1024, "shared memory of the main kernel");
         if ((e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)smem)) != cudaSuccess) {
             *what = "smem attribute";
@@ -811,7 +938,7 @@ static cudaError_t launch_d(const Args& a, void* workspace, cudaStream_t s, std:
         dim3 g2(a.hkv, a.batch, (a.max_seqlen_k + BN - 1) / BN);
         for (int half = 0; half < D / DH; ++half) {  // one pass per 64 output columns
             p.dhalf = half;
-            bwd_main_kernel<D><<<g2, kThreads, smem, s>>>(tq, tk, tv, tdo, tdq, p);
+            bwd_main_kernel<D><<<g2, kThreads, smem, s>>>(tq, tk, tv, tdo, tdq, trec, p);
             if ((e = cudaGetLastError()) != cudaSuccess) {
                 *what = "main launch";
                 return e;

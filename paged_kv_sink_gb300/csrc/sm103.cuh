@@ -281,6 +281,19 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
     return d;
 }
 
+// Shared-memory matrix descriptor for a K-major operand in the 32-byte-swizzled
+// layout: rows of 32 bytes (16 bf16 of K: one k-step), 8-row atoms of 256 bytes
+// (SBO = 256; the tile 256-byte aligned).  The swizzle exchanges the two 16-byte
+// halves of the rows whose index has bit 2 set.
+__device__ __forceinline__ uint64_t sdesc_sw32(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)(256u >> 4) << 32;
+    d |= (uint64_t)1u << 46;  // descriptor version for tcgen05
+    d |= (uint64_t)6u << 61;  // 32-byte swizzle
+    return d;
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16 with bf16 A/B and fp32 D.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
     return (1u << 4)                               // D: f32
