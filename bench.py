@@ -45,8 +45,8 @@ NCU_TRAFFIC = {
     "fwd_kernel/extend_window": {"src": "be9e0f6a91f4c9cf", "bytes": 757_656_320},
     # fwd_kernel<64> reading K/V through a page-16 table: 448.7 MB + 259.3 MB
     "fwd_kernel/extend_paged": {"src": "be9e0f6a91f4c9cf", "bytes": 707_991_552},
-    # bwd_main_kernel<64>: 2.428 GB read + 1.090 GB written per launch
-    "bwd_main_kernel/train": {"src": "5ff263e6c2749d8f", "bytes": 3_518_621_952},
+    # bwd_main_kernel<64>: 2.779 GB read + 1.065 GB written per launch
+    "bwd_main_kernel/train": {"src": "d23d9814e7edfda7", "bytes": 3_844_050_688},
     # decode_split_kernel: 1.943 GB + 0.011 GB
     "decode/decode_sink": {"src": "c0d40bc40087f07f", "bytes": 1_954_153_216},
     # decode_split_kernel: 1.074 GB + 0.007 GB

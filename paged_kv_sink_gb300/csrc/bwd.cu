@@ -22,14 +22,16 @@
 //    The per-query terms ride in the GEMMs: one more 16-wide k-step multiplies
 //    a block of ones (keys x 16) by the tile's 128 records (TMA-loaded with Q
 //    and dO), each holding -LSE / scale and -D of a query split into three bf16
-//    parts, so S^T comes out as S - LSE / scale and dP^T as dP - D.  Two warpgroups share
-//    the elementwise work: thread = (key, half of the 128 query columns), with
-//    no per-query data to fetch.  P^T and dS^T go to TMEM as bf16 pairs and dS
-//    to shared memory once (the MN-major A of dQ); the previous step's dQ tile
-//    is added to an fp32 accumulator with TMA bulk tensor reduce-adds.  dK / dV
-//    are summed over the group in TMEM (no atomics); dS leaves out the softmax
-//    scale, which dK and dQ take on their way out.
-//  * bwd_dq_convert_kernel: fp32 dQ accumulator -> bf16.
+//    parts, so S^T comes out as S - LSE / scale and dP^T as dP - D.  Sixteen
+//    warps: a producer, two MMA issuers and a dQ reducer; two warpgroups for
+//    the elementwise work (thread = key x half of the 128 query columns, no
+//    per-query data to fetch), which write P^T and dS^T to TMEM as bf16 pairs
+//    and dS to shared memory once (the MN-major A of dQ); and one warpgroup
+//    that moves each dQ tile from TMEM to a staging buffer, from where TMA
+//    bulk tensor reduce-adds add it to an fp32 accumulator.  dK / dV are summed
+//    over the group in TMEM (no atomics); dS leaves out the softmax scale,
+//    which dK and dQ take on their way out.
+//  * bwd_dq_convert_kernel: fp32 dQ accumulator times the softmax scale -> bf16.
 #include <cudaTypedefs.h>
 
 #include "bwd.h"
@@ -44,10 +46,14 @@ using namespace sm103;
 constexpr int BM = 128;  // query rows per tile
 constexpr int BN = 128;  // keys per CTA
 constexpr int DH = 64;   // output columns of dQ / dK / dV per main-kernel pass
-constexpr int kThreads = 384;
-constexpr int kRegsCtrl = 104;
-constexpr int kRegsWork = 200;  // 128*104 + 256*200 = 64512 = 384 * 168
-constexpr int kWork = 256;      // elementwise threads: warps 4..11
+constexpr int kThreads = 512;
+// Registers per thread after the role split (the launch gives 128 to each of the
+// 512 threads): 128 * 136 + 256 * 160 + 128 * 56 = 65536.
+constexpr int kRegsCtrl = 136;   // warps 0..3: producer, MMA issuers, dQ reducer
+constexpr int kRegsWork = 160;   // warps 4..11: elementwise
+constexpr int kRegsStage = 56;   // warps 12..15: dQ stagers
+constexpr int kWork = 256;       // elementwise threads
+constexpr int kStage = 128;      // dQ stager threads
 constexpr uint32_t kTile = 128 * 128;  // one 128-byte-swizzled atom: 128 rows x 128 bytes
 // Head-dim dependent sizes.  A 128-row operand tile of Q, dO, K or V is D / 64
 // atoms (atom a: elements 64a .. 64a + 63 of every row, at byte offset
@@ -63,11 +69,13 @@ struct Cfg {
 };
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns.  Lane = key for S^T, dP^T (fp32, column = query), dV, dK (fp32
-// accumulators over the whole loop) and P^T (bf16 pairs: column c holds queries
-// 2c and 2c + 1); lane = query for dQ (fp32, one step).  dS^T (bf16 pairs) is
-// written over the dP^T columns its thread has already read: the query half h
-// at cDP + 64 h, 32 columns.
-constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDK = 320, cDQ = 384, cPT = 448;
+// accumulators over the whole loop) and dS^T (bf16 pairs: column c holds
+// queries 2c and 2c + 1); lane = query for dQ (fp32, one step).  P^T (bf16
+// pairs) is written over the dP^T columns its thread has already read: the
+// query half h at cDP + 64 h, 32 columns.  So the next S^T waits only for the
+// elementwise warps to read this one, and the next dP^T for dV, which leaves
+// it a whole P computation of slack.
+constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDK = 320, cDQ = 384, cDS = 448;
 // One 128-row K-major operand of a single k-step (16 bf16 = 32 bytes per row) in
 // the 32-byte-swizzled layout.
 constexpr uint32_t kAug = 128 * 32;
@@ -96,11 +104,13 @@ struct __align__(1024) Smem {
     uint64_t kv_ready;  // K / V rows past the request's last key zeroed (tail key tiles only)
     uint64_t qdo_tail;  // a head's last query tile reaching past the request lands here first
     uint64_t qdo_full[kQStages], qdo_empty[kQStages];
-    uint64_t s_full, s_free, dp_full;           // per step: S^T read out, dP^T
-    uint64_t p_full;                            // P^T in TMEM (and the previous dQ read out)
-    uint64_t ds_full, mma2_done;                // dS^T / dS written; dK and dQ done
-    uint64_t dq_staged;     // all elementwise threads wrote their part of the dQ tile
-    uint64_t dq_stage_free; // the bulk reduce has finished reading the staging buffer
+    uint64_t s_full, dp_full;     // per step: S^T / dP^T in TMEM
+    uint64_t s_free, p_full;      // S^T read out; dP^T read out and P^T written over it
+    uint64_t pv_done;             // dV has read P^T (the dP^T columns are free again)
+    uint64_t ds_full, mma2_done;  // dS^T / dS written; dK and dQ done
+    uint64_t dq_read;             // the stagers have read dQ out of TMEM
+    uint64_t dq_staged;           // the stagers have written the dQ tile
+    uint64_t dq_stage_free;       // the bulk reduce has finished reading the staging buffer
     uint64_t final_bar;  // dV / dK / dQ issuer done
     uint64_t final_sdp;  // S^T / dP^T issuer done
     uint32_t tmem_base;
@@ -240,12 +250,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&S.qdo_empty[s], 1);
         }
         mbar_init(&S.s_full, 1);
-        mbar_init(&S.s_free, kWork);
         mbar_init(&S.dp_full, 1);
-        mbar_init(&S.p_full, kWork);
-        mbar_init(&S.ds_full, kWork);
+        // the elementwise and stager warps arrive once per warp
+        mbar_init(&S.s_free, kWork / 32);
+        mbar_init(&S.p_full, kWork / 32);
+        mbar_init(&S.pv_done, 1);
+        mbar_init(&S.ds_full, kWork / 32);
         mbar_init(&S.mma2_done, 1);
-        mbar_init(&S.dq_staged, kWork);
+        mbar_init(&S.dq_read, kStage / 32);
+        mbar_init(&S.dq_staged, kStage / 32);
         mbar_init(&S.dq_stage_free, 1);
         mbar_init(&S.final_bar, 1);
         mbar_init(&S.final_sdp, 1);
@@ -263,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort = &S.abort;
 
     if (warp < 4) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtrl));
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsCtrl));
         if (warp == 0) {
             // -------------------------------------------------------- producer
             // (converged warp: every lane waits, lane 0 issues the copies)
@@ -308,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             bool ok = true;
             if (kv_tail) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&S.kv_full, 0, abort));
+                ok = mbar_wait_warp(&S.kv_full, 0, abort);
                 if (ok) {
                     zero_rows(S.k, Lk - j0);
                     zero_rows(S.v, Lk - j0);
@@ -323,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (; ok && t < T; ++t) {
                 const int st = t % kQStages;
                 if (t >= kQStages &&
-                    !__all_sync(0xffffffffu, mbar_wait(&S.qdo_empty[st], (t / kQStages - 1) & 1, abort)))
+                    !mbar_wait_warp(&S.qdo_empty[st], (t / kQStages - 1) & 1, abort))
                     break;
                 const int h = kvh * p.group + g_c;
                 const int q0 = (qr.lo + qt_c) * BM;
@@ -338,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tail_last = tail ? (tail_last | (1u << st)) : (tail_last & ~(1u << st));
                 if (tail) {
                     tail_pending = true;
-                    if (!__all_sync(0xffffffffu, mbar_wait(&S.qdo_tail, tails & 1, abort))) break;
+                    if (!mbar_wait_warp(&S.qdo_tail, tails & 1, abort)) break;
                     tail_pending = false;
                     ++tails;
                     zero_rows(S.q[st], Lq - q0);
@@ -369,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // accumulator with TMA bulk tensor reduce-adds, then frees the stage.
             int g_c = 0, qt_c = 0;
             for (int tt = 0; tt < T; ++tt) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&S.dq_staged, tt & 1, abort))) break;
+                if (!mbar_wait_warp(&S.dq_staged, tt & 1, abort)) break;
                 if (lane == 0) {
                     const int hh = kvh * p.group + g_c;
                     const int qq0 = (qr.lo + qt_c) * BM;
@@ -390,12 +403,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if ((warp == 1 || warp == 3) && T > 0) {
             // -------------------------------------------------------- MMA issuers
             // Two issuing warps feed the tensor core independent instruction
-            // streams: warp 1 issues each step's S^T as soon as the elementwise
-            // warps have read the previous one, and dP^T once dK has read the
-            // previous dS^T (which sits in the dP^T columns); warp 3 issues dV
-            // once P^T is in TMEM, then dK / dQ once dS^T / dS are written.  Both
-            // run converged (every lane waits; elect.sync picks the issuing lane),
-            // and dK / dQ are interleaved k-step by k-step.
+            // streams: warp 1 issues each step's S^T once the elementwise warps
+            // have read the previous one, and dP^T once dV has read the previous
+            // P^T (written over the dP^T columns); warp 3 issues dV once P^T is in
+            // TMEM, then dK / dQ once dS^T / dS are written and the stagers have
+            // read the previous dQ.  Both run converged (every lane waits;
+            // elect.sync picks the issuing lane), and dK / dQ are interleaved
+            // k-step by k-step.
             constexpr uint32_t idSS = idesc_bf16_f32(BN, BM, false, false);  // S^T, dP^T: both K-major
             constexpr uint32_t idKV = idesc_bf16_f32(BN, DH, false, true);   // dV, dK: A in TMEM, B (dO, Q) MN-major
             constexpr uint32_t idQ = idesc_bf16_f32(BM, DH, true, true);     // dQ: A (dS) and B (K) MN-major
@@ -407,9 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t d_ones_d = sdesc_sw32(smem_u32(S.ones_d));          // ... and of dP^T
             const uint64_t dk_mn = sdesc_sw128(smem_u32(S.k), 8192, 1024) + half_off;  // K, MN-major (B of dQ)
             const uint64_t ds_mn = sdesc_sw128(smem_u32(S.dsb), kTile, 1024);  // dS, MN-major (A of dQ)
-            auto wait_all = [&](uint64_t* bar, uint32_t parity) {
-                return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
-            };
+            auto wait_all = [&](uint64_t* bar, uint32_t parity) { return mbar_wait_warp(bar, parity, abort); };
             bool ok = wait_all(kv_tail ? &S.kv_ready : &S.kv_full, 0);
             if (warp == 1) {
                 for (int t = 0; ok && t < T; ++t) {
@@ -419,21 +431,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     const uint64_t dq_k = sdesc_sw128(smem_u32(S.q[st]), 16, 1024);
                     const uint64_t ddo_k = sdesc_sw128(smem_u32(S.dout[st]), 16, 1024);
+                    const uint64_t drec = sdesc_sw32(smem_u32(S.rec[st]));
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {  // 16 head-dim elements = 32 bytes per k-step
                         const uint32_t o = (kk >> 2) * (kTile >> 4) + (kk & 3) * 2;  // atom kk / 4
                         umma_ss_e(tmem + cS, dk_k + o, dq_k + o, idSS, kk > 0);
                     }
-                    umma_ss_e(tmem + cS, d_ones_lse, sdesc_sw32(smem_u32(S.rec[st])), idSS, 1u);  // - LSE / scale
+                    umma_ss_e(tmem + cS, d_ones_lse, drec, idSS, 1u);  // - LSE / scale
                     umma_commit_e(&S.s_full);
-                    if (t > 0 && !(ok = wait_all(&S.mma2_done, (t - 1) & 1))) break;
+                    if (t > 0 && !(ok = wait_all(&S.pv_done, (t - 1) & 1))) break;
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t o = (kk >> 2) * (kTile >> 4) + (kk & 3) * 2;
                         umma_ss_e(tmem + cDP, dv_k + o, ddo_k + o, idSS, kk > 0);
                     }
-                    umma_ss_e(tmem + cDP, d_ones_d, sdesc_sw32(smem_u32(S.rec[st])), idSS, 1u);  // - D
+                    umma_ss_e(tmem + cDP, d_ones_d, drec, idSS, 1u);  // - D
                     umma_commit_e(&S.dp_full);
                 }
                 // Every MMA this warp issued must be complete before TMEM is released.
@@ -445,21 +458,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = wait_all(&S.p_full, t & 1))) break;
                     tc_fence_after();
                     const uint64_t ddo_mn = sdesc_sw128(smem_u32(S.dout[st]), 8192, 1024) + half_off;
-                    // dV: k-step kk runs over queries 16 kk .. 16 kk + 15 (P^T: 8 TMEM
-                    // columns per step; MN-major dO: 2048 bytes per step)
+                    // dV: k-step kk runs over queries 16 kk .. 16 kk + 15 (P^T of query
+                    // half kk / 4 sits at cDP + 64 (kk / 4), 8 columns per step;
+                    // MN-major dO: 2048 bytes per step)
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        umma_ts_e(tmem + cDV, tmem + cPT + kk * 8, ddo_mn + 128 * kk, idKV, (t > 0 || kk > 0) ? 1u : 0u);
-                    // dS^T / dS written
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t a_p = tmem + cDP + 64 * (kk >> 2) + 8 * (kk & 3);
+                        umma_ts_e(tmem + cDV, a_p, ddo_mn + 128 * kk, idKV, (t > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit_e(&S.pv_done);
                     if (!(ok = wait_all(&S.ds_full, t & 1))) break;
+                    if (t > 0 && !(ok = wait_all(&S.dq_read, (t - 1) & 1))) break;
                     tc_fence_after();
                     const uint64_t dq_mn = sdesc_sw128(smem_u32(S.q[st]), 8192, 1024) + half_off;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        // dK: queries 16 kk .. 16 kk + 15; dS^T of query half kk / 4 sits at
-                        // cDP + 64 (kk / 4), 8 columns per step
-                        const uint32_t a_ds = tmem + cDP + 64 * (kk >> 2) + 8 * (kk & 3);
-                        umma_ts_e(tmem + cDK, a_ds, dq_mn + 128 * kk, idKV, (t > 0 || kk > 0) ? 1u : 0u);
+                        // dK: queries 16 kk .. 16 kk + 15 (dS^T: 8 columns per step)
+                        umma_ts_e(tmem + cDK, tmem + cDS + 8 * kk, dq_mn + 128 * kk, idKV, (t > 0 || kk > 0) ? 1u : 0u);
                         // dQ: keys 16 kk .. 16 kk + 15 (2048 bytes into the MN-major dS and K alike)
                         umma_ss_e(tmem + cDQ, ds_mn + 128 * kk, dk_mn + 128 * kk, idQ, kk > 0);
                     }
@@ -470,12 +485,59 @@ __global__ void __launch_bounds__(kThreads, 1)
                 drain_wait(&S.final_bar, 0);
             }
         }
+    } else if (warp >= 12) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsStage));
+        // ------------------------------------------------------------ dQ stagers
+        // Lane = query row r of the tile (TMEM lane of dQ).  Each step's dQ tile
+        // (its GEMM complete) is read out of TMEM 16 columns at a time and
+        // written to the staging buffer (two 32-column fp32 halves, 128-byte
+        // swizzled rows); warp 2 adds it to the fp32 accumulator with TMA bulk
+        // reduce-adds.  Query rows past the request's end (another request's
+        // rows) are staged as zeros: their dS is zero, but times a non-finite key
+        // it would not be.  The softmax scale is applied when the accumulator is
+        // converted.
+        const int r = (warp & 3) * 32 + lane;
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        int g_c = 0, qt_c = 0;
+        for (int t = 0; t < T; ++t) {
+            const int q0 = (qr.lo + qt_c) * BM;
+            bool ok = mbar_wait_warp(&S.mma2_done, t & 1, abort);
+            // the bulk reduce of step t - 1 has finished reading the stage
+            ok = ok && (t == 0 || mbar_wait_warp(&S.dq_stage_free, (t - 1) & 1, abort));
+            if (!ok) break;
+            tc_fence_after();
+            const bool valid = q0 + r < Lq;
+#pragma unroll
+            for (int c16 = 0; c16 < 4; ++c16) {  // columns 16 c16 .. 16 c16 + 15
+                uint32_t u[16];
+                tmem_ld16(tmem + lane_base + cDQ + 16 * c16, u);
+                tmem_ld_wait();
+                if (c16 == 3) {  // dQ is out of TMEM: the next step's dQ GEMM may overwrite it
+                    tc_fence_before();
+                    mbar_arrive_warp(&S.dq_read);
+                }
+                uint8_t* row = S.dq_stage[c16 >> 1] + r * 128;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int chunk = (c16 & 1) * 4 + c;  // 16-byte chunk of the 128-byte row
+                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(smem_u32(row) + ((chunk ^ (r & 7)) << 4)),
+                                 "r"(valid ? u[4 * c] : 0u), "r"(valid ? u[4 * c + 1] : 0u),
+                                 "r"(valid ? u[4 * c + 2] : 0u), "r"(valid ? u[4 * c + 3] : 0u)
+                                 : "memory");
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive_warp(&S.dq_staged);
+            if (++qt_c == nqt) {
+                qt_c = 0;
+                ++g_c;
+            }
+        }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsWork));
         // ------------------------------------------------------------ elementwise
-        // Lane = key r of the CTA (TMEM lane of S^T, dP^T, P^T, dS^T, dV, dK) and
-        // query row r of the tile (TMEM lane of dQ); hh = query half: columns
-        // 64 hh .. 64 hh + 63 of S^T / dP^T, dQ columns 32 hh .. 32 hh + 31.
+        // Lane = key r of the CTA (TMEM lane of S^T, dP^T, P^T, dS^T, dV, dK); hh =
+        // query half: columns 64 hh .. 64 hh + 63 of S^T / dP^T.
         const int q4 = warp & 3;
         const int hh = (warp - 4) >> 2;
         const int r = q4 * 32 + lane;
@@ -485,49 +547,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kpos = j0 + r;
         bool ok = true;
 
-        // The dQ tile of step tt (its GEMMs complete) leaves through shared memory:
-        // this lane's query row, 32 columns (half hh), is loaded from TMEM while the
-        // step's dS is stored, then staged times the softmax scale (dS leaves it
-        // out); warp 2 adds the staged tile to the fp32 accumulator with TMA bulk
-        // reduce-adds.
-        uint32_t* const stage_row = reinterpret_cast<uint32_t*>(S.dq_stage[hh] + r * 128);
-        // Query rows past the request's end (another request's rows) are staged as
-        // zeros: their dS is zero, but times a non-finite key it would not be.
-        const uint64_t scx2 = f2_pack(p.scale, p.scale);
-        auto stage_dq = [&](uint32_t (&u)[32], int q0_row) {
-            const bool valid = q0_row + r < Lq;
-#pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-                float a, b;
-                f2_unpack(f2_mul(f2_pack(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), scx2), a, b);
-                u[c] = valid ? __float_as_uint(a) : 0u;
-                u[c + 1] = valid ? __float_as_uint(b) : 0u;
-            }
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(smem_u32(stage_row) + (((c ^ (r & 7))) << 4)),
-                             "r"(u[4 * c]), "r"(u[4 * c + 1]), "r"(u[4 * c + 2]), "r"(u[4 * c + 3])
-                             : "memory");
-            }
-        };
-
         // step t = g_c * nqt + qt_c (head g_c of the group, query tile qt_c)
         int g_c = 0, qt_c = 0;
-        int q0_prev = 0;  // first query row of the previous step's tile
         for (int t = 0; t < T; ++t) {
             const int q0 = (qr.lo + qt_c) * BM;
-            ok = mbar_wait(&S.s_full, t & 1, abort);
-            if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
-            }
+            if (!(ok = mbar_wait_warp(&S.s_full, t & 1, abort))) break;
             tc_fence_after();
             uint32_t pa[32], pb[32];  // S^T, then P (fp32), of this key's queries 0..31 / 32..63 of the half
             tmem_ld32(tmem + lane_base + cS + 64 * hh, pa);
             tmem_ld32(tmem + lane_base + cS + 64 * hh + 32, pb);
             tmem_ld_wait();
             tc_fence_before();
-            mbar_arrive(&S.s_free);
+            mbar_arrive_warp(&S.s_free);  // S^T read: the next step's S^T may overwrite it
             // Columns e (queries q0 + 64 hh + e) that see this key: lo <= e <= hi.
             // Query position pos sees key kpos iff kpos < Lk, kpos <= pos (causal)
             // and (kpos < F or kpos >= pos + 1 - W) (window); the columns past the
@@ -551,44 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 p_cols<true, 0>(pa, sc2, lo, hi, pw);
                 p_cols<true, 32>(pb, sc2, lo, hi, pw);
             }
-            if (t > 0) {
-                // dV, dK and dQ of the previous step are done: P^T, dS^T (in the dP^T
-                // columns, which dP^T of this step overwrote after that) and dS are
-                // free again, and dQ of the previous step is ready
-                ok = mbar_wait(&S.mma2_done, (t - 1) & 1, abort);
-                if (!__all_sync(0xffffffffu, ok)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-            }
-            tmem_st32(tmem + lane_base + cPT + 32 * hh, pw);
-            if (t > 0) {
-                uint32_t u[32];  // dQ of step t - 1, out of TMEM before this step's dQ GEMM
-                tmem_ld32(tmem + lane_base + cDQ + hh * 32, u);
-                tmem_ld_wait();
-                tmem_st_wait();
-                tc_fence_before();
-                mbar_arrive(&S.p_full);
-                // the bulk reduce of step t - 2 has finished reading the stage
-                ok = t == 1 || mbar_wait(&S.dq_stage_free, (t - 2) & 1, abort);
-                if (!__all_sync(0xffffffffu, ok)) {
-                    ok = false;
-                    break;
-                }
-                stage_dq(u, q0_prev);
-                fence_proxy_async_smem();
-                mbar_arrive(&S.dq_staged);
-            } else {
-                tmem_st_wait();
-                tc_fence_before();
-                mbar_arrive(&S.p_full);
-            }
-            ok = mbar_wait(&S.dp_full, t & 1, abort);
-            if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
-            }
+            if (!(ok = mbar_wait_warp(&S.dp_full, t & 1, abort))) break;
             tc_fence_after();
             uint32_t dw[32];  // dS / scale of this key's 64 queries, bf16 pairs
             {
@@ -601,13 +595,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ds_cols<true, 0>(pa, dr, lo, hi, dw);
                 tmem_ld32(tmem + lane_base + cDP + 64 * hh + 32, dr);
                 tmem_ld_wait();
+                // P^T over this thread's dP^T columns (all read now): the A of dV
+                tmem_st32(tmem + lane_base + cDP + 64 * hh, pw);
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive_warp(&S.p_full);
                 if (full)
                     ds_cols<false, 32>(pb, dr, lo, hi, dw);
                 else
                     ds_cols<true, 32>(pb, dr, lo, hi, dw);
             }
-            // dS^T into this thread's dP^T columns (read above): the A of dK
-            tmem_st32(tmem + lane_base + cDP + 64 * hh, dw);
+            if (t > 0) {  // dK and dQ of the previous step are done with dS^T and dS
+                if (!(ok = mbar_wait_warp(&S.mma2_done, (t - 1) & 1, abort))) break;
+                tc_fence_after();
+            }
+            // dS^T: the A of dK
+            tmem_st32(tmem + lane_base + cDS + 32 * hh, dw);
             // dS row r (64 queries = atom hh, chunks 0..7 of 16 bytes): the A of dQ
 #pragma unroll
             for (int cc = 0; cc < 8; ++cc) {
@@ -619,31 +622,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&S.ds_full);
-            q0_prev = q0;
+            mbar_arrive_warp(&S.ds_full);
             if (++qt_c == nqt) {
                 qt_c = 0;
                 ++g_c;
             }
         }
-        // last step's dQ, then dK (query half 0) / dV (query half 1)
-        if (ok && T > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&S.mma2_done, (T - 1) & 1, abort));
-            if (ok) {
-                tc_fence_after();
-                uint32_t u[32];
-                tmem_ld32(tmem + lane_base + cDQ + hh * 32, u);
-                tmem_ld_wait();
-                ok = __all_sync(0xffffffffu, T == 1 || mbar_wait(&S.dq_stage_free, (T - 2) & 1, abort));
-                if (ok) {
-                    stage_dq(u, q0_prev);
-                    fence_proxy_async_smem();
-                    mbar_arrive(&S.dq_staged);
-                }
-            }
-        }
-        if (ok && T > 0) ok = mbar_wait(&S.final_bar, 0, abort);
-        ok = __all_sync(0xffffffffu, ok);
+        // dK (query half 0) / dV (query half 1)
+        if (ok && T > 0) ok = mbar_wait_warp(&S.final_bar, 0, abort);
         const bool have = ok && T > 0;
         if (have) tc_fence_after();
         const size_t rowoff =
@@ -766,13 +752,15 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
     }
 }
 
-// acc holds rows of row4 float4 (hq * 64 / 4); dq rows are dq_rs4 uint2 apart.
+// acc holds rows of row4 float4 (hq * d / 4); dq rows are dq_rs4 uint2 apart.  The
+// accumulator holds sum dS K with dS short of the softmax scale.
 __global__ void bwd_dq_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq, size_t n4,
-                                      int row4, long long dq_rs4) {
+                                      int row4, long long dq_rs4, float scale) {
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
         const float4 v = acc[i];
         const size_t row = i / (size_t)row4, c = i - row * (size_t)row4;
-        dq[row * (size_t)dq_rs4 + c] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+        dq[row * (size_t)dq_rs4 + c] =
+            make_uint2(pack_bf16x2(v.x * scale, v.y * scale), pack_bf16x2(v.z * scale, v.w * scale));
     }
 }
 
@@ -951,7 +939,8 @@ static cudaError_t launch_d(const Args& a, void* workspace, cudaStream_t s, std:
         if (blocks > 152 * 16) blocks = 152 * 16;
         const long long dq_rs = a.dq_rs > 0 ? a.dq_rs : (long long)a.hq * D;
         bwd_dq_convert_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(dq_accum),
-                                                    reinterpret_cast<uint2*>(a.dq), n4, a.hq * D / 4, dq_rs / 4);
+                                                    reinterpret_cast<uint2*>(a.dq), n4, a.hq * D / 4, dq_rs / 4,
+                                                    a.scale);
         if ((e = cudaGetLastError()) != cudaSuccess) {
             *what = "dq convert launch";
             return e;
