@@ -517,7 +517,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
     ap.add_argument("--only", default=None,
                     choices=["decode_sink", "decode_window", "train", "extend_paged", "decode_append",
-                             "extend_window"],
+                             "extend_window", "extend_varlen"],
                     help="run one secondary workload alone and print its line (for profiling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -553,10 +553,11 @@ def main():
             r = bench_extend_paged(torch, ext, dev, w, args.steps, args.warmup, flush, peaks, peak_src)
         elif args.only == "decode_append":
             r = bench_decode_append(torch, ext, dev, w, args.steps, args.warmup, flush, peaks, peak_src)
-        elif args.only == "extend_window":
+        elif args.only in ("extend_window", "extend_varlen"):
             ms, flops, roof, _ = bench_extend(torch, ext, dev, w, args.steps, args.warmup, flush, peaks, peak_src)
-            r = {"metric": "attn TFLOP/s (visible pairs)", "value": roof["achieved"], "unit": "TFLOP/s",
-                 "ms_per_step": ms, "algorithmic_tflop_per_step": flops / 1e12, "roofline": roof}
+            r = {"metric": "attn TFLOP/s (visible pairs)" if args.only == "extend_window" else "attn TFLOP/s",
+                 "value": roof["achieved"], "unit": "TFLOP/s", "ms_per_step": ms,
+                 "algorithmic_tflop_per_step": flops / 1e12, "roofline": roof}
         else:
             r = bench_decode(torch, ext, dev, w, args.steps, args.warmup, flush, peaks, peak_src)
         check_status(ext, args.only)

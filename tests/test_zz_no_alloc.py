@@ -1,4 +1,7 @@
-"""The allocation-free decode entry point against the allocating one.
+"""The allocation-free decode entry point against the allocating one and the
+oracle (paged decode, sink and first/last window: sglang PR "To implement
+attention-sink", Motivation; the sink term: flash-attention PR "feat: Implement
+Sink Attention", Key Changes).
 
 Some callers cannot allocate device memory when they call into the library
 (an engine that reserved the GPU up front, a latency-critical path that must
@@ -10,6 +13,7 @@ process and after every other test.
 import pytest
 import torch
 
+from oracle import attn_sink_oracle as orc
 from paged_kv_sink_gb300 import workloads as wl
 from parity import assert_lse_close, assert_out_close
 
@@ -44,12 +48,18 @@ def test_noalloc_matches_allocating_entry_point_twice(ext, case):
     (q, kc, vc, pt, sl), sink = _dev(dc)
     ref_o, ref_l = ext.attn_sink_decode_paged(q, kc, vc, pt, sl, sink, dc.win_first, dc.win_last)
     torch.cuda.synchronize()
+    # the oracle on every request of the small case, on three requests (all heads) of the large one
+    reqs = list(range(dc.q.shape[0])) if case == "fits" else [0, 31, 63]
+    O, LSE = orc.attn_decode_paged(dc.q, dc.k_cache, dc.v_cache, dc.page_table, dc.seqlens, dc.page_size,
+                                   dc.sink, dc.win_first, dc.win_last, requests=reqs)
     for _ in range(2):  # two calls in a row share (and reuse) the static scratch
         o, l = ext.attn_sink_decode_paged_noalloc(q, kc, vc, pt, sl, sink, dc.win_first, dc.win_last)
         torch.cuda.synchronize()
         assert ext.device_status() == 0
         assert_out_close(o.cpu(), ref_o.cpu())
         assert_lse_close(l.cpu(), ref_l.cpu())
+        assert_out_close(o.cpu()[reqs], O[reqs], "out vs oracle")
+        assert_lse_close(l.cpu()[reqs], LSE[reqs], "lse vs oracle")
 
 
 def test_noalloc_rejects_oversized_requests(ext):
