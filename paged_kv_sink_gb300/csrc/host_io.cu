@@ -1,16 +1,25 @@
 // Forward attention on host-resident tensors with the transfers pipelined
 // against the kernels (a native runtime piece around the forward kernel).
 //
-// The batch is processed request by request on library-owned streams:
-//   copy-in stream   host -> device rows of request r (q, k, v)
-//   compute streams  the forward kernel of request r (two streams, alternating,
-//                    so that the grids of consecutive requests overlap)
-//   copy-out stream  device -> host rows of out and lse of request r
-// chained with events, so the copies of request r + 1 and of request r - 1
-// overlap the kernel of request r.  Everything is asynchronous; the caller's
-// stream waits for the last copy.  Host buffers should be page-locked
-// (cudaHostAlloc / cudaHostRegister): copies from pageable memory are
-// synchronous with the host and do not overlap.
+// The batch is processed in chunks of up to 1024 query rows on library-owned
+// streams.  A chunk of rows i0 .. i1 of a request sees only the keys before
+// off + i1 (off = Lk - Lq, bottom-right causal alignment), so it runs as a
+// one-request forward over those rows and that key prefix, with the same
+// alignment, and only the K/V rows its prefix adds have to arrive first:
+//   copy-in stream   host -> device: the chunk's q rows and its new k, v rows
+//   compute streams  the forward kernel of the chunk (two streams, alternating,
+//                    so that the grids of consecutive chunks overlap)
+//   copy-out stream  device -> host rows of out and lse of the chunk
+// chained with events, so the copies of the next and of the previous chunk
+// overlap the kernel of this one, and the first kernel starts after one
+// chunk's rows instead of a whole request's.  Requests go in the order
+// Johnson's rule gives for the two-stage flow shop copy-in -> kernel (first
+// those whose copy-in is shorter than their kernel, by increasing copy-in
+// time, then the others by decreasing kernel time).  Everything is
+// asynchronous; the caller's stream waits for the last copy.  Host buffers
+// should be page-locked (cudaHostAlloc / cudaHostRegister): copies from
+// pageable memory are synchronous with the host and do not overlap.
+#include <algorithm>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -26,6 +35,66 @@ namespace hostio {
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr int kChunkRows = 1024;
+
+// One chunk: query rows [qb, qe) and keys [kb, ke) (absolute row offsets).
+struct Chunk {
+    int qb, qe, kb, ke;
+};
+
+// The chunks in processing order (see the file comment).
+std::vector<Chunk> plan_chunks(const Args& a) {
+    const size_t q_row = (size_t)a.hq * a.head_dim * 2, kv_row = (size_t)a.hkv * a.head_dim * 2;
+    // Stage times, estimated from the bytes a request moves in (at ~200 GB/s) and
+    // the (query, key) pairs its kernel visits (at ~1.1 PFLOP/s); only their
+    // ratios and order matter.
+    struct Job {
+        int r;
+        double in, comp;
+    };
+    std::vector<Job> jobs;
+    for (int r = 0; r < a.batch; ++r) {
+        const long long Lq = a.cu_q[r + 1] - a.cu_q[r], Lk = std::max(0, a.cu_k[r + 1] - a.cu_k[r]);
+        if (Lq <= 0) continue;
+        double pairs = (double)Lq * (double)Lk;
+        if (a.causal) {
+            const long long off = Lk - Lq;
+            pairs = 0.0;
+            for (long long i = 0; i < Lq; i += 64) {  // rows i .. i + 63 see about min(Lk, off + i + 32) keys
+                const long long n = std::min(64LL, Lq - i);
+                pairs += (double)n * (double)std::max(0LL, std::min(Lk, off + i + 32));
+            }
+        }
+        if (a.win_last > 0) pairs = std::min(pairs, (double)Lq * (double)(a.win_first + a.win_last));
+        const double bytes_in = (double)Lq * q_row + 2.0 * (double)Lk * kv_row;
+        jobs.push_back({r, bytes_in / 200e9, pairs * a.hq * 4.0 * a.head_dim / 1.1e15});
+    }
+    std::stable_sort(jobs.begin(), jobs.end(), [](const Job& x, const Job& y) {
+        const bool fx = x.in <= x.comp, fy = y.in <= y.comp;
+        if (fx != fy) return fx;
+        return fx ? x.in < y.in : x.comp > y.comp;
+    });
+    std::vector<Chunk> chunks;
+    for (const Job& job : jobs) {
+        const int q0 = a.cu_q[job.r], Lq = a.cu_q[job.r + 1] - q0;
+        const int k0 = a.cu_k[job.r], Lk = std::max(0, a.cu_k[job.r + 1] - k0);
+        for (int i0 = 0; i0 < Lq; i0 += kChunkRows) {
+            const int i1 = std::min(Lq, i0 + kChunkRows);
+            const int need = a.causal ? std::max(0, std::min(Lk, Lk - Lq + i1)) : Lk;
+            chunks.push_back({q0 + i0, q0 + i1, k0, k0 + need});
+        }
+    }
+    return chunks;
+}
+
+int count_chunks(const Args& a) {
+    int n = 0;
+    for (int r = 0; r < a.batch; ++r) {
+        const int Lq = a.cu_q[r + 1] - a.cu_q[r];
+        if (Lq > 0) n += (Lq + kChunkRows - 1) / kChunkRows;
+    }
+    return n;
+}
 
 struct Streams {
     cudaStream_t in = nullptr, out = nullptr, comp[2] = {nullptr, nullptr};
@@ -90,12 +159,14 @@ cudaError_t run(const Args& a, void* dev_buf, cudaStream_t caller, std::string* 
     char* dout = carve((size_t)a.total_q * q_row);
     float* dlse = reinterpret_cast<float*>(carve((size_t)a.hq * a.total_q * 4));
     float* dsink = a.sink ? reinterpret_cast<float*>(carve((size_t)a.hq * 4)) : nullptr;
-    int32_t* dcu_q = reinterpret_cast<int32_t*>(carve((size_t)(a.batch + 1) * 4));
-    int32_t* dcu_k = reinterpret_cast<int32_t*>(carve((size_t)(a.batch + 1) * 4));
+    const std::vector<Chunk> chunks = plan_chunks(a);
+    const int n_chunks = (int)chunks.size();
+    // per chunk {q begin, q end, k begin, k end}: the cu_seqlens of its one-request launch
+    int32_t* dmeta = reinterpret_cast<int32_t*>(carve((size_t)std::max(1, n_chunks) * 16));
 
     Events evs;
-    cudaEvent_t ready, meta;
-    if ((e = evs.make(&ready)) != cudaSuccess || (e = evs.make(&meta)) != cudaSuccess) {
+    cudaEvent_t ready, meta_in;
+    if ((e = evs.make(&ready)) != cudaSuccess || (e = evs.make(&meta_in)) != cudaSuccess) {
         *what = "events";
         return e;
     }
@@ -109,56 +180,57 @@ cudaError_t run(const Args& a, void* dev_buf, cudaStream_t caller, std::string* 
     const char* hv_ = static_cast<const char*>(a.v);
     char* hout = static_cast<char*>(a.out);
     *what = "copy-in";
-    if ((e = cudaMemcpyAsync(dcu_q, a.cu_q, (size_t)(a.batch + 1) * 4, cudaMemcpyHostToDevice, st.in)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(dcu_k, a.cu_k, (size_t)(a.batch + 1) * 4, cudaMemcpyHostToDevice, st.in)) != cudaSuccess)
+    if (n_chunks > 0 && (e = cudaMemcpyAsync(dmeta, chunks.data(), (size_t)n_chunks * 16, cudaMemcpyHostToDevice,
+                                             st.in)) != cudaSuccess)
         return e;
     if (a.sink && (e = cudaMemcpyAsync(dsink, a.sink, (size_t)a.hq * 4, cudaMemcpyHostToDevice, st.in)) != cudaSuccess)
         return e;
-    if ((e = cudaEventRecord(meta, st.in)) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(meta_in, st.in)) != cudaSuccess) return e;
 
-    int launched = 0;
-    for (int r = 0; r < a.batch; ++r) {
-        const int q0 = a.cu_q[r], q1 = a.cu_q[r + 1], k0 = a.cu_k[r], k1 = a.cu_k[r + 1];
-        const int Lq = q1 - q0, Lk = k1 - k0;
-        if (Lq <= 0) continue;
+    int k_have = -1;  // K/V rows of the current request on the device: [kb, k_have)
+    for (int c = 0; c < n_chunks; ++c) {
+        const Chunk& ch = chunks[c];
+        if (c == 0 || chunks[c - 1].kb != ch.kb || chunks[c - 1].qe != ch.qb) k_have = ch.kb;  // a new request
         *what = "copy-in";
-        if ((e = cudaMemcpyAsync(dq + (size_t)q0 * q_row, hq_ + (size_t)q0 * q_row, (size_t)Lq * q_row,
-                                 cudaMemcpyHostToDevice, st.in)) != cudaSuccess)
+        if ((e = cudaMemcpyAsync(dq + (size_t)ch.qb * q_row, hq_ + (size_t)ch.qb * q_row,
+                                 (size_t)(ch.qe - ch.qb) * q_row, cudaMemcpyHostToDevice, st.in)) != cudaSuccess)
             return e;
-        if (Lk > 0 && ((e = cudaMemcpyAsync(dk + (size_t)k0 * kv_row, hk_ + (size_t)k0 * kv_row, (size_t)Lk * kv_row,
-                                            cudaMemcpyHostToDevice, st.in)) != cudaSuccess ||
-                       (e = cudaMemcpyAsync(dv + (size_t)k0 * kv_row, hv_ + (size_t)k0 * kv_row, (size_t)Lk * kv_row,
-                                            cudaMemcpyHostToDevice, st.in)) != cudaSuccess))
+        if (ch.ke > k_have &&
+            ((e = cudaMemcpyAsync(dk + (size_t)k_have * kv_row, hk_ + (size_t)k_have * kv_row,
+                                  (size_t)(ch.ke - k_have) * kv_row, cudaMemcpyHostToDevice, st.in)) != cudaSuccess ||
+             (e = cudaMemcpyAsync(dv + (size_t)k_have * kv_row, hv_ + (size_t)k_have * kv_row,
+                                  (size_t)(ch.ke - k_have) * kv_row, cudaMemcpyHostToDevice, st.in)) != cudaSuccess))
             return e;
+        k_have = std::max(k_have, ch.ke);
         cudaEvent_t in_done, comp_done;
         if ((e = evs.make(&in_done)) != cudaSuccess || (e = evs.make(&comp_done)) != cudaSuccess) {
             *what = "events";
             return e;
         }
         if ((e = cudaEventRecord(in_done, st.in)) != cudaSuccess) return e;
-        cudaStream_t cs = st.comp[launched & 1];
-        ++launched;
-        if ((e = cudaStreamWaitEvent(cs, meta, 0)) != cudaSuccess || (e = cudaStreamWaitEvent(cs, in_done, 0)) != cudaSuccess)
+        cudaStream_t cs = st.comp[c & 1];
+        if ((e = cudaStreamWaitEvent(cs, meta_in, 0)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(cs, in_done, 0)) != cudaSuccess)
             return e;
         prefill::FwdArgs f = {};
         f.q = dq;
         f.k = dk;
         f.v = dv;
         f.sink = dsink;
-        f.cu_q = dcu_q + r;  // this request alone: cu[r], cu[r + 1] are absolute row offsets
-        f.cu_k = dcu_k + r;
+        f.cu_q = dmeta + 4 * c;  // this chunk alone: absolute row offsets
+        f.cu_k = dmeta + 4 * c + 2;
         f.out = dout;
         f.lse = a.lse ? dlse : nullptr;
         f.batch = 1;
         f.total_q = a.total_q;  // also the lse head stride
-        // K/V rows past this request are out of the tensor for this launch (the
+        // K/V rows past the chunk's keys are out of the tensor for this launch (the
         // copy engine may still be writing them): the tail tile reads zeros.
-        f.total_k = k1;
+        f.total_k = ch.ke;
         f.hq = a.hq;
         f.hkv = a.hkv;
         f.head_dim = a.head_dim;
-        f.max_seqlen_q = Lq;
-        f.max_seqlen_k = Lk;
+        f.max_seqlen_q = ch.qe - ch.qb;
+        f.max_seqlen_k = ch.ke - ch.kb;
         f.win_first = a.win_first;
         f.win_last = a.win_last;
         f.causal = a.causal;
@@ -167,11 +239,12 @@ cudaError_t run(const Args& a, void* dev_buf, cudaStream_t caller, std::string* 
         if ((e = cudaEventRecord(comp_done, cs)) != cudaSuccess) return e;
         *what = "copy-out";
         if ((e = cudaStreamWaitEvent(st.out, comp_done, 0)) != cudaSuccess) return e;
-        if ((e = cudaMemcpyAsync(hout + (size_t)q0 * q_row, dout + (size_t)q0 * q_row, (size_t)Lq * q_row,
-                                 cudaMemcpyDeviceToHost, st.out)) != cudaSuccess)
+        if ((e = cudaMemcpyAsync(hout + (size_t)ch.qb * q_row, dout + (size_t)ch.qb * q_row,
+                                 (size_t)(ch.qe - ch.qb) * q_row, cudaMemcpyDeviceToHost, st.out)) != cudaSuccess)
             return e;
-        if (a.lse && (e = cudaMemcpy2DAsync(a.lse + q0, (size_t)a.total_q * 4, dlse + q0, (size_t)a.total_q * 4,
-                                            (size_t)Lq * 4, a.hq, cudaMemcpyDeviceToHost, st.out)) != cudaSuccess)
+        if (a.lse && (e = cudaMemcpy2DAsync(a.lse + ch.qb, (size_t)a.total_q * 4, dlse + ch.qb, (size_t)a.total_q * 4,
+                                            (size_t)(ch.qe - ch.qb) * 4, a.hq, cudaMemcpyDeviceToHost, st.out)) !=
+                          cudaSuccess)
             return e;
     }
     // The caller's stream (and the release of the scratch on it) waits for every copy.
@@ -189,7 +262,7 @@ size_t scratch_bytes(const Args& a) {
     auto r = [](size_t b) { return (b + 255) & ~size_t(255); };
     const size_t q_row = (size_t)a.hq * a.head_dim * 2, kv_row = (size_t)a.hkv * a.head_dim * 2;
     return 2 * r((size_t)a.total_q * q_row) + 2 * r((size_t)a.total_k * kv_row) + r((size_t)a.hq * a.total_q * 4) +
-           r((size_t)a.hq * 4) + 2 * r((size_t)(a.batch + 1) * 4);
+           r((size_t)a.hq * 4) + r((size_t)std::max(1, count_chunks(a)) * 16);
 }
 
 }  // namespace hostio
