@@ -303,9 +303,8 @@ int attn_sink_fwd_paged(const attn_bf16* q, const attn_bf16* k_new, const attn_b
  *                of each KV head)
  *   dsink        (hq,) fp32; must be non-NULL iff sink is non-NULL; written
  *                (not accumulated)
- * Supported: head_dim 64 or 128 (at 128 the main kernel runs in two passes,
- * each recomputing S and dP and producing 64 columns of dq, dk, dv);
- * hq % hkv == 0.  A request's gradients depend on
+ * Supported: head_dim 64 or 128 (one pass each: 128-row query steps at 64,
+ * 64-row steps at 128); hq % hkv == 0.  A request's gradients depend on
  * its own rows only: the rows that its last query or key tile covers past its
  * own (another request's, or past total_q / total_k) are replaced by zeros in
  * shared memory, so they may hold anything, NaN included.

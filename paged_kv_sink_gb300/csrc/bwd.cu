@@ -30,7 +30,9 @@
 //    that moves each dQ tile from TMEM to a staging buffer, from where TMA
 //    bulk tensor reduce-adds add it to an fp32 accumulator.  dK / dV are summed
 //    over the group in TMEM (no atomics); dS leaves out the softmax scale,
-//    which dK and dQ take on their way out.
+//    which dK and dQ take on their way out.  Head dim 64 runs
+//    bwd_main_kernel (128-row query steps), head dim 128 bwd_main128_kernel
+//    (64-row query steps, so that every product fits TMEM at full width).
 //  * bwd_dq_convert_kernel: fp32 dQ accumulator times the softmax scale -> bf16.
 #include <cudaTypedefs.h>
 
@@ -45,7 +47,7 @@ using namespace sm103;
 
 constexpr int BM = 128;  // query rows per tile
 constexpr int BN = 128;  // keys per CTA
-constexpr int DH = 64;   // output columns of dQ / dK / dV per main-kernel pass
+constexpr int DH = 64;   // head dim of bwd_main_kernel (bwd_main128_kernel takes 128)
 constexpr int kThreads = 512;
 // Registers per thread after the role split (the launch gives 128 to each of the
 // 512 threads): 128 * 136 + 256 * 160 + 128 * 56 = 65536.
@@ -55,17 +57,14 @@ constexpr int kRegsStage = 56;   // warps 12..15: dQ stagers
 constexpr int kWork = 256;       // elementwise threads
 constexpr int kStage = 128;      // dQ stager threads
 constexpr uint32_t kTile = 128 * 128;  // one 128-byte-swizzled atom: 128 rows x 128 bytes
-// Head-dim dependent sizes.  A 128-row operand tile of Q, dO, K or V is D / 64
-// atoms (atom a: elements 64a .. 64a + 63 of every row, at byte offset
-// a * kTile).  At d 128 the products S^T and dP^T run over both atoms, and the
-// main kernel runs twice, each pass producing one 64-column half of dQ, dK and
-// dV (the TMEM budget fits 64 output columns); the Q / dO ring then has one
-// stage to fit shared memory.
+// Sizes of bwd_main_kernel (head dim 64): a 128-row operand tile of Q, dO, K or
+// V is one 128-byte-swizzled atom; the Q / dO ring has three stages.
 template <int D>
 struct Cfg {
-    static constexpr int kAtoms = D / 64;
-    static constexpr uint32_t kOp = kTile * kAtoms;
-    static constexpr int kQStages = D == 64 ? 3 : 1;
+    static_assert(D == 64, "bwd_main_kernel is the head-dim-64 kernel");
+    static constexpr int kAtoms = 1;
+    static constexpr uint32_t kOp = kTile;
+    static constexpr int kQStages = 3;
 };
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns.  Lane = key for S^T, dP^T (fp32, column = query), dV, dK (fp32
@@ -120,14 +119,12 @@ struct __align__(1024) Smem {
 struct MainParams {
     const int32_t* cu_q;
     const int32_t* cu_k;
-    float* dq_accum;       // (total_q, hq, d) fp32
     __nv_bfloat16* dk;     // (total_k, hkv, d), rows dk_rs elements apart
     __nv_bfloat16* dv;     // rows dv_rs elements apart
     long long dk_rs, dv_rs;
     int hq, hkv, group, total_q, total_k;
     int win_first, win_last, causal;
     float scale, scale_log2;
-    int dhalf;  // output columns 64 * dhalf .. + 63 of dQ, dK, dV (d 128: two passes)
 };
 
 // Loads one 128-row operand tile (D / 64 atoms) starting at `row`.
@@ -142,14 +139,14 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     mbar_wait(bar, parity, &dummy);
 }
 
-// Query tiles of one head that see at least one key of [j0, j0 + BN).
+// Query tiles (of `rows` rows) of one head that see at least one key of [j0, j0 + BN).
 struct QRange {
     int lo, hi;  // tile indices [lo, hi)
 };
 
-__device__ __forceinline__ QRange query_tiles(int j0, int Lq, int Lk, int causal, int F, int W) {
+__device__ __forceinline__ QRange query_tiles(int j0, int Lq, int Lk, int causal, int F, int W, int rows = BM) {
     QRange r;
-    const int nqt = (Lq + BM - 1) / BM;
+    const int nqt = (Lq + rows - 1) / rows;
     const int off = Lk - Lq;
     int row_lo = 0, row_hi = Lq;  // query rows [row_lo, row_hi)
     if (causal) row_lo = max(0, j0 - off);  // pos >= j0
@@ -161,8 +158,8 @@ __device__ __forceinline__ QRange query_tiles(int j0, int Lq, int Lk, int causal
         r.lo = r.hi = 0;
         return r;
     }
-    r.lo = row_lo / BM;
-    r.hi = min(nqt, (row_hi + BM - 1) / BM);
+    r.lo = row_lo / rows;
+    r.hi = min(nqt, (row_hi + rows - 1) / rows);
     return r;
 }
 
@@ -386,8 +383,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     const int hh = kvh * p.group + g_c;
                     const int qq0 = (qr.lo + qt_c) * BM;
-                    tma_reduce_add_3d(&tm_dq, S.dq_stage[0], p.dhalf * DH, hh, q_start + qq0);
-                    tma_reduce_add_3d(&tm_dq, S.dq_stage[1], p.dhalf * DH + 32, hh, q_start + qq0);
+                    tma_reduce_add_3d(&tm_dq, S.dq_stage[0], 0, hh, q_start + qq0);
+                    tma_reduce_add_3d(&tm_dq, S.dq_stage[1], 32, hh, q_start + qq0);
                     bulk_commit_group();
                     bulk_wait_read_all();
                     mbar_arrive(&S.dq_stage_free);
@@ -413,13 +410,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idSS = idesc_bf16_f32(BN, BM, false, false);  // S^T, dP^T: both K-major
             constexpr uint32_t idKV = idesc_bf16_f32(BN, DH, false, true);   // dV, dK: A in TMEM, B (dO, Q) MN-major
             constexpr uint32_t idQ = idesc_bf16_f32(BM, DH, true, true);     // dQ: A (dS) and B (K) MN-major
-            const uint32_t half_off = (uint32_t)p.dhalf * (kTile >> 4);      // this pass's 64-column atom
             // Descriptor bases; a k-step adds its byte offset / 16 to the address field.
             const uint64_t dk_k = sdesc_sw128(smem_u32(S.k), 16, 1024);        // K, K-major (A of S^T)
             const uint64_t dv_k = sdesc_sw128(smem_u32(S.v), 16, 1024);        // V, K-major (A of dP^T)
             const uint64_t d_ones_lse = sdesc_sw32(smem_u32(S.ones_lse));      // A of the extra k-step of S^T
             const uint64_t d_ones_d = sdesc_sw32(smem_u32(S.ones_d));          // ... and of dP^T
-            const uint64_t dk_mn = sdesc_sw128(smem_u32(S.k), 8192, 1024) + half_off;  // K, MN-major (B of dQ)
+            const uint64_t dk_mn = sdesc_sw128(smem_u32(S.k), 8192, 1024);     // K, MN-major (B of dQ)
             const uint64_t ds_mn = sdesc_sw128(smem_u32(S.dsb), kTile, 1024);  // dS, MN-major (A of dQ)
             auto wait_all = [&](uint64_t* bar, uint32_t parity) { return mbar_wait_warp(bar, parity, abort); };
             bool ok = wait_all(kv_tail ? &S.kv_ready : &S.kv_full, 0);
@@ -457,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int st = t % kQStages;
                     if (!(ok = wait_all(&S.p_full, t & 1))) break;
                     tc_fence_after();
-                    const uint64_t ddo_mn = sdesc_sw128(smem_u32(S.dout[st]), 8192, 1024) + half_off;
+                    const uint64_t ddo_mn = sdesc_sw128(smem_u32(S.dout[st]), 8192, 1024);
                     // dV: k-step kk runs over queries 16 kk .. 16 kk + 15 (P^T of query
                     // half kk / 4 sits at cDP + 64 (kk / 4), 8 columns per step;
                     // MN-major dO: 2048 bytes per step)
@@ -470,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = wait_all(&S.ds_full, t & 1))) break;
                     if (t > 0 && !(ok = wait_all(&S.dq_read, (t - 1) & 1))) break;
                     tc_fence_after();
-                    const uint64_t dq_mn = sdesc_sw128(smem_u32(S.q[st]), 8192, 1024) + half_off;
+                    const uint64_t dq_mn = sdesc_sw128(smem_u32(S.q[st]), 8192, 1024);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         // dK: queries 16 kk .. 16 kk + 15 (dS^T: 8 columns per step)
@@ -633,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool have = ok && T > 0;
         if (have) tc_fence_after();
         const size_t rowoff =
-            (size_t)(k_start + kpos) * (size_t)(hh == 0 ? p.dk_rs : p.dv_rs) + (size_t)kvh * D + p.dhalf * DH;
+            (size_t)(k_start + kpos) * (size_t)(hh == 0 ? p.dk_rs : p.dv_rs) + (size_t)kvh * D;
         const uint32_t col = hh == 0 ? cDK : cDV;
         __nv_bfloat16* outp = hh == 0 ? p.dk : p.dv;
         const float f = hh == 0 ? p.scale : 1.f;  // dK takes the softmax scale that dS left out
@@ -649,6 +645,475 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (kpos < Lk) {
                 uint4* dst = reinterpret_cast<uint4*>(outp + rowoff + half * 32);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(u[8 * c + 0]) * f, __uint_as_float(u[8 * c + 1]) * f);
+                    w.y = pack_bf16x2(__uint_as_float(u[8 * c + 2]) * f, __uint_as_float(u[8 * c + 3]) * f);
+                    w.z = pack_bf16x2(__uint_as_float(u[8 * c + 4]) * f, __uint_as_float(u[8 * c + 5]) * f);
+                    w.w = pack_bf16x2(__uint_as_float(u[8 * c + 6]) * f, __uint_as_float(u[8 * c + 7]) * f);
+                    dst[c] = w;
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Head dim 128 in one pass: bwd_main128_kernel.  The same roles, barriers and
+// per-query k-step as bwd_main_kernel, with steps of 64 query rows so that
+// TMEM holds every product at full width: S^T 64 columns, dP^T 64 (P^T written
+// over it), dV 128, dK 128, dS^T 32 and dQ^T = K^T dS^T 64 (lane = head dim,
+// column = query), 480 of 512.  dQ^T leaves through the staging buffer by
+// transposed stores (lane = head dim, so a warp writes one 128-byte query row
+// per store).
+namespace d128 {
+constexpr int BQ = 64;                      // query rows per step
+constexpr int kQS = 3;                      // Q / dO / record stages
+constexpr uint32_t kQAtom = BQ * 128;       // 64 rows x 128 bytes (64 head dims)
+constexpr uint32_t kQTile = 2 * kQAtom;     // 64 rows x 128 head dims
+constexpr uint32_t kKTile = 2 * kTile;      // 128 keys x 128 head dims
+constexpr uint32_t kDqBox = BQ * 128;       // 64 query rows x 32 head dims fp32
+constexpr uint32_t kRecTile = BQ * 32;      // 64 records
+// TMEM columns: lane = key for S^T, dP^T, dV, dK, dS^T; lane = head dim for dQ^T.
+constexpr uint32_t cS = 0, cDP = 64, cDV = 128, cDK = 256, cDS = 384, cDQ = 448;
+
+struct __align__(1024) Smem {
+    uint8_t k[kKTile];
+    uint8_t v[kKTile];
+    uint8_t q[kQS][kQTile];
+    uint8_t dout[kQS][kQTile];
+    uint8_t dsb[kTile];             // dS: 128 key rows x 64 queries (one atom), the MN-major B of dQ^T
+    uint8_t dq_stage[4][kDqBox];    // dQ tile: four 32-dim boxes of 64 query rows, 128-byte swizzled
+    uint8_t ones_lse[kAug];
+    uint8_t ones_d[kAug];
+    uint8_t rec[kQS][kRecTile];
+    uint64_t kv_full, kv_ready, qdo_tail;
+    uint64_t qdo_full[kQS], qdo_empty[kQS];
+    uint64_t s_full, dp_full, s_free, p_full, pv_done, ds_full, mma2_done;
+    uint64_t dq_read, dq_staged, dq_stage_free;
+    uint64_t final_bar, final_sdp;
+    uint32_t tmem_base;
+    int abort;
+};
+
+__device__ __forceinline__ void tma_q(uint8_t* dst, const CUtensorMap* m, uint64_t* bar, int head, int row) {
+    tma_load_3d(dst, m, bar, 0, head, row);
+    tma_load_3d(dst + kQAtom, m, bar, 64, head, row);
+}
+__device__ __forceinline__ void tma_k(uint8_t* dst, const CUtensorMap* m, uint64_t* bar, int head, int row) {
+    tma_load_3d(dst, m, bar, 0, head, row);
+    tma_load_3d(dst + kTile, m, bar, 64, head, row);
+}
+}  // namespace d128
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_main128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_rec,
+                       const MainParams p) {
+    using d128::BQ;
+    using d128::kQS;
+    using d128::kQAtom;
+    using d128::kQTile;
+    using d128::kKTile;
+    using d128::kRecTile;
+    using d128::tma_q;
+    using d128::tma_k;
+    constexpr uint32_t cS = d128::cS, cDP = d128::cDP, cDV = d128::cDV, cDK = d128::cDK, cDS = d128::cDS,
+                       cDQ = d128::cDQ;
+    constexpr int D = 128;
+    extern __shared__ uint8_t smem_raw[];
+    d128::Smem& S = *reinterpret_cast<d128::Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kvh = blockIdx.x, b = blockIdx.y, kt = blockIdx.z;
+
+    const int q_start = p.cu_q[b];
+    int Lq = p.cu_q[b + 1] - q_start;
+    const int k_start = p.cu_k[b];
+    int Lk = p.cu_k[b + 1] - k_start;
+    if (q_start + Lq > p.total_q || k_start + Lk > p.total_k || Lq < 0 || Lk < 0) {
+        if (threadIdx.x == 0 && kt == 0 && kvh == 0) raise_status(ATTN_SINK_DEV_SEQLEN_OOB);
+        Lq = max(0, min(Lq, p.total_q - q_start));
+        Lk = max(0, min(Lk, p.total_k - k_start));
+    }
+    const int j0 = kt * BN;
+    if (j0 >= Lk) return;
+    const int off = Lk - Lq;
+    const QRange qr = query_tiles(j0, Lq, Lk, p.causal, p.win_first, p.win_last, BQ);
+    const int nqt = qr.hi - qr.lo;
+    const int T = nqt * p.group;  // steps: (head g, 64-row query tile)
+    const bool kv_tail = j0 + BN > Lk;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&S.kv_full, 1);
+        mbar_init(&S.kv_ready, 1);
+        mbar_init(&S.qdo_tail, 1);
+        for (int s = 0; s < kQS; ++s) {
+            mbar_init(&S.qdo_full[s], 1);
+            mbar_init(&S.qdo_empty[s], 1);
+        }
+        mbar_init(&S.s_full, 1);
+        mbar_init(&S.dp_full, 1);
+        mbar_init(&S.s_free, kWork / 32);
+        mbar_init(&S.p_full, kWork / 32);
+        mbar_init(&S.pv_done, 1);
+        mbar_init(&S.ds_full, kWork / 32);
+        mbar_init(&S.mma2_done, 1);
+        mbar_init(&S.dq_read, kStage / 32);
+        mbar_init(&S.dq_staged, kStage / 32);
+        mbar_init(&S.dq_stage_free, 1);
+        mbar_init(&S.final_bar, 1);
+        mbar_init(&S.final_sdp, 1);
+        S.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&S.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = S.tmem_base;
+    volatile int* abort = &S.abort;
+
+    if (warp < 4) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsCtrl));
+        if (warp == 0) {
+            // -------------------------------------------------------- producer
+            // As in bwd_main_kernel: K / V once, then each step's Q, dO and
+            // records; rows past the request's keys / queries are zeroed in shared
+            // memory before the tensor core reads them.
+            auto zero_rows = [&](uint8_t* atom, int r0, int nrows) {
+                uint4* t4 = reinterpret_cast<uint4*>(atom);
+                for (int c = r0 * 8 + lane; c < nrows * 8; c += 32) t4[c] = make_uint4(0u, 0u, 0u, 0u);
+            };
+            if (lane == 0) {
+                prefetch_tmap(&tm_q);
+                prefetch_tmap(&tm_k);
+                prefetch_tmap(&tm_v);
+                prefetch_tmap(&tm_do);
+                prefetch_tmap(&tm_rec);
+                mbar_expect_tx(&S.kv_full, 2 * kKTile);
+                tma_k(S.k, &tm_k, &S.kv_full, kvh, k_start + j0);
+                tma_k(S.v, &tm_v, &S.kv_full, kvh, k_start + j0);
+            }
+            {
+                // the two ones blocks (see bwd_main_kernel)
+                const uint4 one = make_uint4(0x3F803F80u, 0x00003F80u, 0u, 0u);
+                const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+                for (int c = lane; c < (int)(kAug / 16); c += 32) {
+                    const int j = c >> 1, half = (c & 1) ^ ((j >> 2) & 1);
+                    reinterpret_cast<uint4*>(S.ones_lse)[c] = half == 0 ? one : zero;
+                    reinterpret_cast<uint4*>(S.ones_d)[c] = half == 1 ? one : zero;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            bool ok = true;
+            if (kv_tail) {
+                ok = mbar_wait_warp(&S.kv_full, 0, abort);
+                if (ok) {
+                    for (int a = 0; a < 2; ++a) {
+                        zero_rows(S.k + a * kTile, Lk - j0, BN);
+                        zero_rows(S.v + a * kTile, Lk - j0, BN);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&S.kv_ready);
+                }
+            }
+            int t = 0, g_c = 0, qt_c = 0, tails = 0;
+            bool tail_pending = false;
+            uint32_t tail_last = 0;
+            for (; ok && t < T; ++t) {
+                const int st = t % kQS;
+                if (t >= kQS && !mbar_wait_warp(&S.qdo_empty[st], (t / kQS - 1) & 1, abort)) break;
+                const int h = kvh * p.group + g_c;
+                const int q0 = (qr.lo + qt_c) * BQ;
+                const bool tail = q0 + BQ > Lq;
+                uint64_t* bar = tail ? &S.qdo_tail : &S.qdo_full[st];
+                if (lane == 0) {
+                    mbar_expect_tx(bar, 2 * kQTile + kRecTile);
+                    tma_q(S.q[st], &tm_q, bar, h, q_start + q0);
+                    tma_q(S.dout[st], &tm_do, bar, h, q_start + q0);
+                    tma_load_3d(S.rec[st], &tm_rec, bar, 0, h, q_start + q0);
+                }
+                tail_last = tail ? (tail_last | (1u << st)) : (tail_last & ~(1u << st));
+                if (tail) {
+                    tail_pending = true;
+                    if (!mbar_wait_warp(&S.qdo_tail, tails & 1, abort)) break;
+                    tail_pending = false;
+                    ++tails;
+                    for (int a = 0; a < 2; ++a) {
+                        zero_rows(S.q[st] + a * kQAtom, Lq - q0, BQ);
+                        zero_rows(S.dout[st] + a * kQAtom, Lq - q0, BQ);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&S.qdo_full[st]);
+                }
+                if (++qt_c == nqt) {
+                    qt_c = 0;
+                    ++g_c;
+                }
+            }
+            if (lane == 0) {
+                drain_wait(&S.kv_full, 0);
+                if (tail_pending) drain_wait(&S.qdo_tail, tails & 1);
+                for (int st = 0; st < kQS; ++st) {
+                    const int n = t > st ? (t - st + kQS - 1) / kQS : 0;
+                    if (n > 0 && !((tail_last >> st) & 1u)) drain_wait(&S.qdo_full[st], (n - 1) & 1);
+                }
+            }
+            __syncwarp();
+        } else if (warp == 2 && T > 0) {
+            // -------------------------------------------------------- dQ reducer
+            int g_c = 0, qt_c = 0;
+            for (int tt = 0; tt < T; ++tt) {
+                if (!mbar_wait_warp(&S.dq_staged, tt & 1, abort)) break;
+                if (lane == 0) {
+                    const int hh = kvh * p.group + g_c;
+                    const int qq0 = (qr.lo + qt_c) * BQ;
+#pragma unroll
+                    for (int bx = 0; bx < 4; ++bx) tma_reduce_add_3d(&tm_dq, S.dq_stage[bx], 32 * bx, hh, q_start + qq0);
+                    bulk_commit_group();
+                    bulk_wait_read_all();
+                    mbar_arrive(&S.dq_stage_free);
+                }
+                __syncwarp();
+                if (++qt_c == nqt) {
+                    qt_c = 0;
+                    ++g_c;
+                }
+            }
+            if (lane == 0) bulk_wait_all();
+            __syncwarp();
+        } else if ((warp == 1 || warp == 3) && T > 0) {
+            // -------------------------------------------------------- MMA issuers
+            constexpr uint32_t idS = idesc_bf16_f32(BN, BQ, false, false);  // S^T, dP^T: M 128 keys, N 64 queries
+            constexpr uint32_t idKV = idesc_bf16_f32(BN, D, false, true);   // dV, dK: A in TMEM, B MN-major, N 128
+            constexpr uint32_t idQ = idesc_bf16_f32(D, BQ, true, true);     // dQ^T: A (K^T) and B (dS) MN-major
+            const uint64_t dk_k = sdesc_sw128(smem_u32(S.k), 16, 1024);
+            const uint64_t dv_k = sdesc_sw128(smem_u32(S.v), 16, 1024);
+            const uint64_t d_ones_lse = sdesc_sw32(smem_u32(S.ones_lse));
+            const uint64_t d_ones_d = sdesc_sw32(smem_u32(S.ones_d));
+            const uint64_t dkT = sdesc_sw128(smem_u32(S.k), kTile, 1024);  // K as the MN-major A of dQ^T (M = head dims)
+            const uint64_t ds_mn = sdesc_sw128(smem_u32(S.dsb), kTile, 1024);
+            bool ok = mbar_wait_warp(kv_tail ? &S.kv_ready : &S.kv_full, 0, abort);
+            if (warp == 1) {
+                for (int t = 0; ok && t < T; ++t) {
+                    const int st = t % kQS;
+                    if (!(ok = mbar_wait_warp(&S.qdo_full[st], (t / kQS) & 1, abort))) break;
+                    if (t > 0 && !(ok = mbar_wait_warp(&S.s_free, (t - 1) & 1, abort))) break;
+                    tc_fence_after();
+                    const uint64_t dq_k = sdesc_sw128(smem_u32(S.q[st]), 16, 1024);
+                    const uint64_t ddo_k = sdesc_sw128(smem_u32(S.dout[st]), 16, 1024);
+                    const uint64_t drec = sdesc_sw32(smem_u32(S.rec[st]));
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {  // 16 head dims per k-step; atom kk / 4
+                        const uint32_t ok_ = (kk >> 2) * (kTile >> 4) + (kk & 3) * 2;
+                        const uint32_t oq = (kk >> 2) * (kQAtom >> 4) + (kk & 3) * 2;
+                        umma_ss_e(tmem + cS, dk_k + ok_, dq_k + oq, idS, kk > 0);
+                    }
+                    umma_ss_e(tmem + cS, d_ones_lse, drec, idS, 1u);  // - LSE / scale
+                    umma_commit_e(&S.s_full);
+                    // P^T of the previous step sits in the dP^T columns until dV has read it
+                    if (t > 0 && !(ok = mbar_wait_warp(&S.pv_done, (t - 1) & 1, abort))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t ok_ = (kk >> 2) * (kTile >> 4) + (kk & 3) * 2;
+                        const uint32_t oq = (kk >> 2) * (kQAtom >> 4) + (kk & 3) * 2;
+                        umma_ss_e(tmem + cDP, dv_k + ok_, ddo_k + oq, idS, kk > 0);
+                    }
+                    umma_ss_e(tmem + cDP, d_ones_d, drec, idS, 1u);  // - D
+                    umma_commit_e(&S.dp_full);
+                }
+                umma_commit_e(&S.final_sdp);
+                drain_wait(&S.final_sdp, 0);
+            } else {
+                for (int t = 0; ok && t < T; ++t) {
+                    const int st = t % kQS;
+                    if (!(ok = mbar_wait_warp(&S.p_full, t & 1, abort))) break;
+                    tc_fence_after();
+                    // dO / Q as MN-major B: N = 128 head dims in two atoms kQAtom apart;
+                    // a k-step (16 queries) is 2048 bytes on
+                    const uint64_t ddo_mn = sdesc_sw128(smem_u32(S.dout[st]), kQAtom, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < BQ / 16; ++kk)  // P^T of query half kk / 2: cDP + 32 (kk / 2), 8 columns per step
+                        umma_ts_e(tmem + cDV, tmem + cDP + 32 * (kk >> 1) + 8 * (kk & 1), ddo_mn + 128 * kk, idKV,
+                                  (t > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit_e(&S.pv_done);
+                    if (!(ok = mbar_wait_warp(&S.ds_full, t & 1, abort))) break;
+                    if (t > 0 && !(ok = mbar_wait_warp(&S.dq_read, (t - 1) & 1, abort))) break;
+                    tc_fence_after();
+                    const uint64_t dq_mn = sdesc_sw128(smem_u32(S.q[st]), kQAtom, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+                        // dQ^T: keys 16 kk .. 16 kk + 15 (2048 bytes into K and dS alike)
+                        umma_ss_e(tmem + cDQ, dkT + 128 * kk, ds_mn + 128 * kk, idQ, kk > 0);
+                        // dK: queries 16 (kk / 2) .. (dS^T 8 columns per step), every other k-step
+                        if ((kk & 1) == 1)
+                            umma_ts_e(tmem + cDK, tmem + cDS + 8 * (kk >> 1), dq_mn + 128 * (kk >> 1), idKV,
+                                      (t > 0 || kk > 1) ? 1u : 0u);
+                    }
+                    umma_commit_e(&S.mma2_done);
+                    umma_commit_e(&S.qdo_empty[st]);
+                }
+                umma_commit_e(&S.final_bar);
+                drain_wait(&S.final_bar, 0);
+            }
+        }
+    } else if (warp >= 12) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsStage));
+        // ------------------------------------------------------------ dQ stagers
+        // Lane = head dim 32 (warp & 3) + lane of dQ^T (TMEM lanes); 16 query
+        // columns at a time, each stored into the query's row of box warp & 3 (a
+        // warp writes one 128-byte row per store).  Queries past the request's end
+        // are staged as zeros.
+        const int box = warp & 3;
+        const uint32_t lane_base = (uint32_t)(box * 32) << 16;
+        uint8_t* const stage = S.dq_stage[box];
+        const uint32_t col = ((uint32_t)(lane >> 2) << 4) | ((uint32_t)(lane & 3) << 2);  // byte in the 128-byte row
+        int g_c = 0, qt_c = 0;
+        for (int t = 0; t < T; ++t) {
+            const int q0 = (qr.lo + qt_c) * BQ;
+            bool ok = mbar_wait_warp(&S.mma2_done, t & 1, abort);
+            ok = ok && (t == 0 || mbar_wait_warp(&S.dq_stage_free, (t - 1) & 1, abort));
+            if (!ok) break;
+            tc_fence_after();
+            const int nvalid = min(BQ, Lq - q0);
+#pragma unroll
+            for (int c16 = 0; c16 < BQ / 16; ++c16) {
+                uint32_t u[16];
+                tmem_ld16(tmem + lane_base + cDQ + 16 * c16, u);
+                tmem_ld_wait();
+                if (c16 == BQ / 16 - 1) {
+                    tc_fence_before();
+                    mbar_arrive_warp(&S.dq_read);
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int c = 16 * c16 + i;  // query row of the box
+                    const uint32_t addr = smem_u32(stage) + c * 128 + (col ^ ((uint32_t)(c & 7) << 4));
+                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(c < nvalid ? u[i] : 0u) : "memory");
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive_warp(&S.dq_staged);
+            if (++qt_c == nqt) {
+                qt_c = 0;
+                ++g_c;
+            }
+        }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsWork));
+        // ------------------------------------------------------------ elementwise
+        // Lane = key r; hh = query half: columns 32 hh .. 32 hh + 31 of the step's
+        // 64 queries.
+        const int q4 = warp & 3;
+        const int hh = (warp - 4) >> 2;
+        const int r = q4 * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+        const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
+        const int F = p.win_first, W = p.win_last;
+        const int kpos = j0 + r;
+        bool ok = true;
+        int g_c = 0, qt_c = 0;
+        for (int t = 0; t < T; ++t) {
+            const int q0 = (qr.lo + qt_c) * BQ;
+            if (!(ok = mbar_wait_warp(&S.s_full, t & 1, abort))) break;
+            tc_fence_after();
+            uint32_t pa[32];  // S^T, then P (fp32), of this key's 32 queries
+            tmem_ld32(tmem + lane_base + cS + 32 * hh, pa);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive_warp(&S.s_free);
+            // columns e (queries q0 + 32 hh + e) that see this key: lo <= e <= hi
+            const long long base = (long long)off + q0 + 32 * hh;
+            int lo = 0;
+            long long hi_ll = (long long)Lq - 1 - q0 - 32 * hh;
+            if (kpos >= Lk) {
+                lo = 32;
+            } else {
+                if (p.causal) lo = (int)max(0LL, min(32LL, (long long)kpos - base));
+                if (W > 0 && kpos >= F) hi_ll = min(hi_ll, (long long)kpos + W - 1 - base);
+            }
+            const int hi = (int)max(-1LL, min(31LL, hi_ll));
+            const bool full = __all_sync(0xffffffffu, lo == 0 && hi == 31);
+            uint32_t pw[32];
+            if (full)
+                p_cols<false, 0>(pa, sc2, lo, hi, pw);
+            else
+                p_cols<true, 0>(pa, sc2, lo, hi, pw);
+            if (!(ok = mbar_wait_warp(&S.dp_full, t & 1, abort))) break;
+            tc_fence_after();
+            uint32_t dw[32];
+            {
+                uint32_t dr[32];
+                tmem_ld32(tmem + lane_base + cDP + 32 * hh, dr);
+                tmem_ld_wait();
+                // P^T over this thread's dP^T columns (read): the A of dV
+                tmem_st16(tmem + lane_base + cDP + 32 * hh, pw);
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive_warp(&S.p_full);
+                if (full)
+                    ds_cols<false, 0>(pa, dr, lo, hi, dw);
+                else
+                    ds_cols<true, 0>(pa, dr, lo, hi, dw);
+            }
+            if (t > 0) {  // dK and dQ^T of the previous step are done with dS^T and dS
+                if (!(ok = mbar_wait_warp(&S.mma2_done, (t - 1) & 1, abort))) break;
+                tc_fence_after();
+            }
+            tmem_st16(tmem + lane_base + cDS + 16 * hh, dw);  // dS^T: the A of dK
+            // dS row r, queries 32 hh .. 32 hh + 31 = 16-byte chunks 4 hh .. 4 hh + 3: the B of dQ^T
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const uint32_t o = sw128_off(r, 4 * hh + cc);
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(smem_u32(S.dsb + o)), "r"(dw[4 * cc]),
+                             "r"(dw[4 * cc + 1]), "r"(dw[4 * cc + 2]), "r"(dw[4 * cc + 3])
+                             : "memory");
+            }
+            fence_proxy_async_smem();
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive_warp(&S.ds_full);
+            if (++qt_c == nqt) {
+                qt_c = 0;
+                ++g_c;
+            }
+        }
+        // dK (query half 0) / dV (query half 1): 128 head dims of key r
+        if (ok && T > 0) ok = mbar_wait_warp(&S.final_bar, 0, abort);
+        const bool have = ok && T > 0;
+        if (have) tc_fence_after();
+        const size_t rowoff = (size_t)(k_start + kpos) * (size_t)(hh == 0 ? p.dk_rs : p.dv_rs) + (size_t)kvh * D;
+        const uint32_t cbase = hh == 0 ? cDK : cDV;
+        __nv_bfloat16* outp = hh == 0 ? p.dk : p.dv;
+        const float f = hh == 0 ? p.scale : 1.f;  // dK takes the softmax scale that dS left out
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t u[32];
+            if (have) {
+                tmem_ld32(tmem + lane_base + cbase + ch * 32, u);
+                tmem_ld_wait();
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) u[e] = 0u;
+            }
+            if (kpos < Lk) {
+                uint4* dst = reinterpret_cast<uint4*>(outp + rowoff + ch * 32);
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint4 w;
@@ -768,9 +1233,11 @@ __global__ void bwd_dq_convert_kernel(const float4* __restrict__ acc, uint2* __r
 // Host side
 
 cudaError_t make_map(CUtensorMap* m, const void* base, int d, int heads, long long rows, std::string* what,
-                     long long row_stride = 0);
-cudaError_t make_map_dq(CUtensorMap* m, const float* base, int d, int heads, long long rows, std::string* what);
-cudaError_t make_map_rec(CUtensorMap* m, const void* base, int heads, long long rows, std::string* what);
+                     long long row_stride = 0, int box_rows = 128);
+cudaError_t make_map_dq(CUtensorMap* m, const float* base, int d, int heads, long long rows, std::string* what,
+                        int box_rows = 128);
+cudaError_t make_map_rec(CUtensorMap* m, const void* base, int heads, long long rows, std::string* what,
+                         int box_rows = 128);
 
 // The fp32 dQ accumulator, then the per-query records (32 bytes per row and head).
 size_t workspace_bytes(const Args& a) {
@@ -792,10 +1259,10 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// (rows, heads, d) bf16 tensor as {d, head, row}; box {64, 1, 128}: one
+// (rows, heads, d) bf16 tensor as {d, head, row}; box {64, 1, box_rows}: one
 // 128-byte-swizzled atom per copy.
 cudaError_t make_map(CUtensorMap* m, const void* base, int D, int heads, long long rows, std::string* what,
-                     long long row_stride) {
+                     long long row_stride, int box_rows) {
     auto fn = encode_fn();
     if (!fn) {
         *what = "cuTensorMapEncodeTiled unavailable";
@@ -803,7 +1270,7 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int D, int heads, long lo
     }
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1)};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)(row_stride > 0 ? row_stride : (long long)D * heads) * 2};
-    cuuint32_t box[3] = {64u, 1, 128};
+    cuuint32_t box[3] = {64u, 1, (cuuint32_t)box_rows};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -815,8 +1282,9 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int D, int heads, long lo
     return cudaSuccess;
 }
 
-// (rows, heads, d) fp32 dQ accumulator as {d, head, row}; box {32, 1, 128}, 128-byte swizzle.
-cudaError_t make_map_dq(CUtensorMap* m, const float* base, int D, int heads, long long rows, std::string* what) {
+// (rows, heads, d) fp32 dQ accumulator as {d, head, row}; box {32, 1, box_rows}, 128-byte swizzle.
+cudaError_t make_map_dq(CUtensorMap* m, const float* base, int D, int heads, long long rows, std::string* what,
+                        int box_rows) {
     auto fn = encode_fn();
     if (!fn) {
         *what = "cuTensorMapEncodeTiled unavailable";
@@ -824,7 +1292,7 @@ cudaError_t make_map_dq(CUtensorMap* m, const float* base, int D, int heads, lon
     }
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1)};
     cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)D * 4 * heads};
-    cuuint32_t box[3] = {32, 1, 128};
+    cuuint32_t box[3] = {32, 1, (cuuint32_t)box_rows};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -836,9 +1304,10 @@ cudaError_t make_map_dq(CUtensorMap* m, const float* base, int D, int heads, lon
     return cudaSuccess;
 }
 
-// (rows, heads, 16) bf16 per-query records as {16, head, row}; box {16, 1, 128},
-// 32-byte swizzle (the layout of the extra k-step's B operand).
-cudaError_t make_map_rec(CUtensorMap* m, const void* base, int heads, long long rows, std::string* what) {
+// (rows, heads, 16) bf16 per-query records as {16, head, row}; box {16, 1,
+// box_rows}, 32-byte swizzle (the layout of the extra k-step's B operand).
+cudaError_t make_map_rec(CUtensorMap* m, const void* base, int heads, long long rows, std::string* what,
+                         int box_rows) {
     auto fn = encode_fn();
     if (!fn) {
         *what = "cuTensorMapEncodeTiled unavailable";
@@ -846,7 +1315,7 @@ cudaError_t make_map_rec(CUtensorMap* m, const void* base, int heads, long long 
     }
     cuuint64_t dims[3] = {(cuuint64_t)kRec, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1)};
     cuuint64_t strides[2] = {(cuuint64_t)kRec * 2, (cuuint64_t)kRec * 2 * heads};
-    cuuint32_t box[3] = {(cuuint32_t)kRec, 1, 128};
+    cuuint32_t box[3] = {(cuuint32_t)kRec, 1, (cuuint32_t)box_rows};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -891,17 +1360,18 @@ static cudaError_t launch_d(const Args& a, void* workspace, cudaStream_t s, std:
         }
     }
     if (a.total_q > 0 && a.total_k > 0 && a.max_seqlen_k > 0) {
+        // query-side boxes: 128 rows per step at d 64, 64 at d 128
+        const int qbox = D == 128 ? d128::BQ : BM;
         CUtensorMap tq, tk, tv, tdo, tdq, trec;
-        if ((e = make_map(&tq, a.q, D, a.hq, a.total_q, what, a.q_rs)) != cudaSuccess) return e;
+        if ((e = make_map(&tq, a.q, D, a.hq, a.total_q, what, a.q_rs, qbox)) != cudaSuccess) return e;
         if ((e = make_map(&tk, a.k, D, a.hkv, a.total_k, what, a.k_rs)) != cudaSuccess) return e;
         if ((e = make_map(&tv, a.v, D, a.hkv, a.total_k, what, a.v_rs)) != cudaSuccess) return e;
-        if ((e = make_map(&tdo, a.dout, D, a.hq, a.total_q, what)) != cudaSuccess) return e;
-        if ((e = make_map_dq(&tdq, dq_accum, D, a.hq, a.total_q, what)) != cudaSuccess) return e;
-        if ((e = make_map_rec(&trec, rec, a.hq, a.total_q, what)) != cudaSuccess) return e;
+        if ((e = make_map(&tdo, a.dout, D, a.hq, a.total_q, what, 0, qbox)) != cudaSuccess) return e;
+        if ((e = make_map_dq(&tdq, dq_accum, D, a.hq, a.total_q, what, qbox)) != cudaSuccess) return e;
+        if ((e = make_map_rec(&trec, rec, a.hq, a.total_q, what, qbox)) != cudaSuccess) return e;
         MainParams p;
         p.cu_q = a.cu_q;
         p.cu_k = a.cu_k;
-        p.dq_accum = dq_accum;
         p.dk = reinterpret_cast<__nv_bfloat16*>(a.dk);
         p.dv = reinterpret_cast<__nv_bfloat16*>(a.dv);
         p.dk_rs = a.dk_rs > 0 ? a.dk_rs : (long long)a.hkv * D;
@@ -916,21 +1386,29 @@ static cudaError_t launch_d(const Args& a, void* workspace, cudaStream_t s, std:
         p.causal = a.causal;
         p.scale = a.scale;
         p.scale_log2 = a.scale * ATTN_LOG2E;
-        const size_t smem = sizeof(Smem<D>) + 1024;
-        static_assert(sizeof(Smem<D>) + 1024 <= 227 * 1024, "shared memory of the main kernel");
-        if ((e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)smem)) != cudaSuccess) {
-            *what = "smem attribute";
-            return e;
-        }
         dim3 g2(a.hkv, a.batch, (a.max_seqlen_k + BN - 1) / BN);
-        for (int half = 0; half < D / DH; ++half) {  // one pass per 64 output columns
-            p.dhalf = half;
-            bwd_main_kernel<D><<<g2, kThreads, smem, s>>>(tq, tk, tv, tdo, tdq, trec, p);
-            if ((e = cudaGetLastError()) != cudaSuccess) {
-                *what = "main launch";
+        if constexpr (D == 128) {
+            const size_t smem = sizeof(d128::Smem) + 1024;
+            static_assert(sizeof(d128::Smem) + 1024 <= 227 * 1024, "shared memory of the d 128 main kernel");
+            if ((e = cudaFuncSetAttribute(bwd_main128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)smem)) != cudaSuccess) {
+                *what = "smem attribute";
                 return e;
             }
+            bwd_main128_kernel<<<g2, kThreads, smem, s>>>(tq, tk, tv, tdo, tdq, trec, p);
+        } else {
+            const size_t smem = sizeof(Smem<D>) + 1024;
+            static_assert(sizeof(Smem<D>) + 1024 <= 227 * 1024, "shared memory of the main kernel");
+            if ((e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)smem)) != cudaSuccess) {
+                *what = "smem attribute";
+                return e;
+            }
+            bwd_main_kernel<D><<<g2, kThreads, smem, s>>>(tq, tk, tv, tdo, tdq, trec, p);
+        }
+        if ((e = cudaGetLastError()) != cudaSuccess) {
+            *what = "main launch";
+            return e;
         }
     }
     if (a.total_q > 0) {
