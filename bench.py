@@ -45,8 +45,10 @@ NCU_TRAFFIC = {
     "fwd_kernel/extend_window": {"src": "be9e0f6a91f4c9cf", "bytes": 757_656_320},
     # fwd_kernel<64> reading K/V through a page-16 table: 448.7 MB + 259.3 MB
     "fwd_kernel/extend_paged": {"src": "be9e0f6a91f4c9cf", "bytes": 707_991_552},
-    # bwd_main_kernel<64>: 2.779 GB read + 1.065 GB written per launch
-    "bwd_main_kernel/train": {"src": "d23d9814e7edfda7", "bytes": 3_844_050_688},
+    # bwd_main_kernel<64>: 2.748 GB read + 1.058 GB written per launch
+    "bwd_main_kernel/train": {"src": "76296cbf95b92602", "bytes": 3_806_221_568},
+    # bwd_main128_kernel on the head-dim-128 training step: 2.676 GB + 1.217 GB
+    "bwd_main128_kernel/train_d128": {"src": "76296cbf95b92602", "bytes": 3_892_545_280},
     # decode_split_kernel: 1.943 GB + 0.011 GB
     "decode/decode_sink": {"src": "c0d40bc40087f07f", "bytes": 1_954_153_216},
     # decode_split_kernel: 1.074 GB + 0.007 GB
@@ -359,14 +361,15 @@ def bench_train(torch, ext, dev, p, steps, warmup, flush, peaks, peak_src):
     bf = 2.5 * ff
     fm, bm = sum(fwd_ms) / steps, sum(bwd_ms) / steps
     total = (ff + bf) / ((fm + bm) * 1e-3) / 1e12
+    main = "bwd_main128_kernel" if p.head_dim == 128 else "bwd_main_kernel"
     bw_ach = bf / (bm * 1e-3) / 1e12
     return {"metric": "attn fwd+bwd TFLOP/s", "value": total, "unit": "TFLOP/s", "ms_per_step": fm + bm,
             "fwd_ms": fm, "bwd_ms": bm, "fwd_tflops": ff / (fm * 1e-3) / 1e12, "bwd_tflops": bw_ach,
             "algorithmic_tflop_per_step": (ff + bf) / 1e12,
-            "roofline": {"kernel": "attn_sink_bwd call (bwd_main_kernel + preprocess + dq convert)",
+            "roofline": {"kernel": f"attn_sink_bwd call ({main} + preprocess + dq convert)",
                          "bound": "tensor", "achieved": bw_ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": bw_ach / peaks["bf16_tflops"], "peak_source": f"bf16 burst, {peak_src}",
-                         "traffic": _traffic("bwd_main_kernel/train", "bwd.cu"),
+                         "traffic": _traffic(f"{main}/" + p.name.split()[0], "bwd.cu"),
                          "algorithmic_flops_per_launch": bf}}
 
 
@@ -517,7 +520,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
     ap.add_argument("--only", default=None,
                     choices=["decode_sink", "decode_window", "train", "extend_paged", "decode_append",
-                             "extend_window", "extend_varlen"],
+                             "extend_window", "extend_varlen", "extend_d128", "train_d128"],
                     help="run one secondary workload alone and print its line (for profiling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -547,13 +550,13 @@ def main():
 
     if args.only:
         w = wl.workload("decode_sink" if args.only == "decode_append" else args.only, seed=0)
-        if args.only == "train":
+        if args.only in ("train", "train_d128"):
             r = bench_train(torch, ext, dev, w, args.steps, args.warmup, flush, peaks, peak_src)
         elif args.only == "extend_paged":
             r = bench_extend_paged(torch, ext, dev, w, args.steps, args.warmup, flush, peaks, peak_src)
         elif args.only == "decode_append":
             r = bench_decode_append(torch, ext, dev, w, args.steps, args.warmup, flush, peaks, peak_src)
-        elif args.only in ("extend_window", "extend_varlen"):
+        elif args.only in ("extend_window", "extend_varlen", "extend_d128"):
             ms, flops, roof, _ = bench_extend(torch, ext, dev, w, args.steps, args.warmup, flush, peaks, peak_src)
             r = {"metric": "attn TFLOP/s (visible pairs)" if args.only == "extend_window" else "attn TFLOP/s",
                  "value": roof["achieved"], "unit": "TFLOP/s", "ms_per_step": ms,

@@ -380,6 +380,23 @@ def train(seed=0):
                         with_dout=True, seed=seed)
 
 
+# Head dim 128 (the width of the models the window form serves): the same
+# lengths as extend_varlen and train with 32 query heads over 8 KV heads.
+def extend_d128(seed=0, n_req=8):
+    def lens(g):
+        prefix = _randint(g, 0, 16384, n_req)
+        chunk = _randint(g, 512, 8192, n_req)
+        return chunk.tolist(), (prefix + chunk).tolist()
+    return make_prefill(name="extend_d128 8req prefix U0-16384 chunk U512-8192 Hq32 Hkv8 d128 sink",
+                        seqlens_q=lens, hq=32, hkv=8, d=128, sink=(-2.0, 4.0), seed=seed)
+
+
+def train_d128(seed=0):
+    return make_prefill(name="train_d128 B2 L8192 Hq32 Hkv8 d128 causal sink fwd+bwd",
+                        seqlens_q=[8192, 8192], hq=32, hkv=8, d=128, sink="normal",
+                        with_dout=True, seed=seed)
+
+
 WORKLOADS = {
     "prefill_tiny": prefill_tiny,
     "extend_varlen": extend_varlen,
@@ -388,6 +405,8 @@ WORKLOADS = {
     "decode_window": decode_window,
     "train": train,
     "extend_paged": extend_paged,
+    "extend_d128": extend_d128,
+    "train_d128": train_d128,
 }
 
 

@@ -109,3 +109,14 @@ def test_train_recipe(no_bulk):
     fwd = bench.fwd_flops(p)
     assert fwd == 2 * 4 * 64 * 64 * (8192 * 8193 // 2)  # 1.10 TFLOP
     assert fwd + 2.5 * fwd == 3_848_760_459_264  # forward + backward (five GEMMs), per step
+
+
+def test_head_dim_128_recipes(no_bulk):
+    """The d-128 bench workloads keep the extend / train lengths at 32 query
+    heads over 8 KV heads."""
+    e, e128 = wl.extend_varlen(), wl.extend_d128()
+    assert e128.seqlens_q == e.seqlens_q and e128.seqlens_k == e.seqlens_k
+    assert (e128.hq, e128.hkv, e128.head_dim) == (32, 8, 128)
+    assert bench.fwd_flops(e128) == bench.fwd_flops(e)  # 4 d Hq per pair: 4*128*32 = 4*64*64
+    t = wl.train_d128()
+    assert t.seqlens_q == [8192, 8192] and (t.hq, t.hkv, t.head_dim) == (32, 8, 128) and t.dout is not None
