@@ -41,6 +41,27 @@ def test_fwd_host_equals_device_entry_point(ext, pinned, d):
     assert_lse_close(lse_h, LSE)
 
 
+@pytest.mark.parametrize("causal,win", [(True, (16, 700)), (False, (0, 0)), (True, (0, 0))])
+def test_fwd_host_multi_chunk_matches_device_and_oracle(ext, causal, win):
+    """Requests longer than one 1024-row chunk, one with fewer keys than queries
+    (its first rows see no key): streaming a request chunk by chunk, each chunk
+    over its key prefix, gives the device entry point's rows bit for bit."""
+    p = wl.make_prefill(seqlens_q=[2500, 1100, 3], seqlens_k=[3000, 900, 50], hq=4, hkv=2, d=64,
+                        sink=(-2.0, 4.0), win_first=win[0], win_last=win[1], causal=causal, seed=5)
+    host = [t.pin_memory() for t in (p.q, p.k, p.v, p.sink, p.cu_seqlens_q, p.cu_seqlens_k)]
+    out_h, lse_h = ext.attn_sink_fwd_host(*host, win_first=win[0], win_last=win[1], causal=causal)
+    torch.cuda.synchronize()
+    assert ext.device_status() == 0
+    d = "cuda"
+    out_d, lse_d = ext.attn_sink_fwd(*[t.to(d) for t in host], p.max_seqlen_q, p.max_seqlen_k, win[0], win[1],
+                                     causal=causal)
+    torch.cuda.synchronize()
+    assert torch.equal(out_h, out_d.cpu()) and torch.equal(lse_h, lse_d.cpu())
+    O, LSE = orc.attn_fwd(p.q, p.k, p.v, p.sink, p.cu_seqlens_q, p.cu_seqlens_k, win[0], win[1], causal=causal)
+    assert_out_close(out_h, O)
+    assert_lse_close(lse_h, LSE)
+
+
 def test_fwd_host_full_size_matches_device(ext):
     """The extend_varlen workload (the bench's end-to-end path), bit-identical to
     the device entry point."""
