@@ -242,13 +242,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
         : "memory");
 }
 
-// Named barrier ID (a compile-time constant, 1..15) over `count` threads (a
-// multiple of 32).
-template <int ID>
-__device__ __forceinline__ void named_bar_sync(uint32_t count) {
-    asm volatile("bar.sync %0, %1;" ::"n"(ID), "r"(count) : "memory");
-}
-
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
