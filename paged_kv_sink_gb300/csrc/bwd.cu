@@ -10,7 +10,8 @@
 // Three kernels:
 //  * bwd_preprocess_kernel: D_i per (row, head) and dsink (warp shuffles, one
 //    fp32 atomic per block and head); it writes each row's -LSE / scale and -D
-//    as a 32-byte record of bf16 parts for the main kernel.
+//    as a 32-byte record of bf16 parts for the main kernel, and clears the
+//    fp32 dQ accumulator.
 //  * bwd_main_kernel (tcgen05): one CTA per (128-key tile, KV head, request);
 //    it loops over the query heads of the KV group and the 128-row query tiles
 //    that see its keys.  Per step five tcgen05 GEMMs, in the key-major
@@ -123,6 +124,7 @@ struct MainParams {
     __nv_bfloat16* dv;     // rows dv_rs elements apart
     long long dk_rs, dv_rs;
     int hq, hkv, group, total_q, total_k;
+    int batch, n_kt;  // requests; key tiles of the longest request
     int win_first, win_last, causal;
     float scale, scale_log2;
 };
@@ -140,6 +142,41 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Query tiles (of `rows` rows) of one head that see at least one key of [j0, j0 + BN).
+// Launch order of the key-tile CTAs (a 1-D grid of hkv * batch * n_kt).  Under
+// causal masking key tile 0 is seen by every query tile and the last one by
+// few, so the long CTAs must start first: tile-major order (key tile slowest)
+// does that.  The CTAs of one (KV head, request) also re-read the same Q / dO
+// tiles and add into the same dQ rows, which stay in L2 only while those CTAs
+// run close together in time; kBand > 0 keeps them together with bands of
+// kBand key tiles taken in increasing order, each band walking the (KV head,
+// request) pairs with the band's key tiles of one pair adjacent, and the last
+// kBand key tiles (the shortest CTAs) tile-major for the tail.  Measured on
+// the B 2 x 8192 causal step: bands of 16 cut the d 64 kernel's DRAM traffic
+// from 3.8 to 3.0 GB but cost it 4 % in time, and gain the d 128 kernel about
+// 1 %, so bwd_main_kernel runs tile-major and bwd_main128_kernel in bands.
+struct CtaTile {
+    int kvh, b, kt;
+};
+template <int kBand>
+__device__ __forceinline__ CtaTile cta_tile(int i, int hkv, int batch, int n_kt) {
+    const int n_grp = hkv * batch;
+    const int tail_from = (kBand > 0 && n_kt > 2 * kBand) ? n_kt - kBand : 0;
+    const int head = tail_from * n_grp;
+    int grp, kt;
+    if (i < head) {
+        const int band = i / (kBand * n_grp);
+        const int wb = min(kBand, tail_from - band * kBand);
+        const int r = i - band * kBand * n_grp;
+        grp = r / wb;
+        kt = band * kBand + r % wb;
+    } else {
+        const int r = i - head;
+        kt = tail_from + r / n_grp;
+        grp = r % n_grp;
+    }
+    return {grp % hkv, grp / hkv, kt};
+}
+
 struct QRange {
     int lo, hi;  // tile indices [lo, hi)
 };
@@ -216,10 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     Smem<D>& S = *reinterpret_cast<Smem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // Grid (KV head, request, key tile) with the key tile slowest: causal key
-    // tile 0 is seen by every query tile, so launching tiles in increasing order
-    // starts the longest CTAs first and leaves short ones for the tail.
-    const int kvh = blockIdx.x, b = blockIdx.y, kt = blockIdx.z;
+    const CtaTile ct = cta_tile<0>(blockIdx.x, p.hkv, p.batch, p.n_kt);
+    const int kvh = ct.kvh, b = ct.b, kt = ct.kt;
 
     const int q_start = p.cu_q[b];
     int Lq = p.cu_q[b + 1] - q_start;
@@ -733,7 +768,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     d128::Smem& S = *reinterpret_cast<d128::Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kvh = blockIdx.x, b = blockIdx.y, kt = blockIdx.z;
+    const CtaTile ct = cta_tile<16>(blockIdx.x, p.hkv, p.batch, p.n_kt);
+    const int kvh = ct.kvh, b = ct.b, kt = ct.kt;
 
     const int q_start = p.cu_q[b];
     int Lq = p.cu_q[b + 1] - q_start;
@@ -1153,15 +1189,23 @@ __device__ __forceinline__ uint4 split3_bf16(float x) {
     return make_uint4(pack_bf16x2(h1, h2), pack_bf16x2(r, 0.f), 0u, 0u);
 }
 
+// Per block: 64 rows of one query head (the head is the fastest grid index, so
+// the blocks in flight read whole rows of O and dO).  Besides D, the records
+// and dsink it clears the block's rows of the fp32 dQ accumulator, and (kv_zero)
+// the whole grid clears the dK / dV rows past the last request's keys.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ out,
                                                              const __nv_bfloat16* __restrict__ dout,
                                                              const float* __restrict__ lse,
                                                              const float* __restrict__ sink, uint4* __restrict__ rec,
-                                                             float* __restrict__ dsink, int total_q, int hq,
-                                                             float scale, const int32_t* __restrict__ cu_q,
-                                                             int batch) {
-    const int h = blockIdx.y;
+                                                             float* __restrict__ dsink, float4* __restrict__ dq_acc,
+                                                             int total_q, int hq, float scale,
+                                                             const int32_t* __restrict__ cu_q,
+                                                             const int32_t* __restrict__ cu_k, int batch,
+                                                             uint4* __restrict__ dk, uint4* __restrict__ dv,
+                                                             int total_k, int hkv, int kv_zero) {
+    const int h = blockIdx.x;
+    const int n_rb = (total_q + 63) / 64;
     // Rows past the last request (cu_q[batch] <= row < total_q) belong to no
     // request: D = 0, a zero record and no sink term, whatever the buffers hold
     // there.
@@ -1170,39 +1214,59 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
     const int sub = tid & 7;
     const float sg = sink ? sink[h] : -INFINITY;
     float acc_sink = 0.f;
-    for (int rr = 0; rr < 2; ++rr) {
-        const int row = blockIdx.x * 64 + rr * 32 + (tid >> 3);
-        float d = 0.f;
-        if (row < rows) {
-            // eight threads per row, D / 8 elements each (16-byte loads)
+    for (int rb = blockIdx.y; rb < n_rb; rb += gridDim.y) {
+        for (int rr = 0; rr < 2; ++rr) {
+            const int row = rb * 64 + rr * 32 + (tid >> 3);
+            float d = 0.f;
+            if (row < rows) {
+                // eight threads per row, D / 8 elements each (16-byte loads)
 #pragma unroll
-            for (int j = 0; j < D / 64; ++j) {
-                const size_t base = ((size_t)row * hq + h) * D + j * 64 + sub * 8;
-                const uint4 o = *reinterpret_cast<const uint4*>(out + base);
-                const uint4 g = *reinterpret_cast<const uint4*>(dout + base);
-                d += bf16_lo(o.x) * bf16_lo(g.x) + bf16_hi(o.x) * bf16_hi(g.x) + bf16_lo(o.y) * bf16_lo(g.y) +
-                     bf16_hi(o.y) * bf16_hi(g.y) + bf16_lo(o.z) * bf16_lo(g.z) + bf16_hi(o.z) * bf16_hi(g.z) +
-                     bf16_lo(o.w) * bf16_lo(g.w) + bf16_hi(o.w) * bf16_hi(g.w);
+                for (int j = 0; j < D / 64; ++j) {
+                    const size_t base = ((size_t)row * hq + h) * D + j * 64 + sub * 8;
+                    const uint4 o = *reinterpret_cast<const uint4*>(out + base);
+                    const uint4 g = *reinterpret_cast<const uint4*>(dout + base);
+                    d += bf16_lo(o.x) * bf16_lo(g.x) + bf16_hi(o.x) * bf16_hi(g.x) + bf16_lo(o.y) * bf16_lo(g.y) +
+                         bf16_hi(o.y) * bf16_hi(g.y) + bf16_lo(o.z) * bf16_lo(g.z) + bf16_hi(o.z) * bf16_hi(g.z) +
+                         bf16_lo(o.w) * bf16_lo(g.w) + bf16_hi(o.w) * bf16_hi(g.w);
+                }
+            }
+            if (row < total_q) {
+                // this row's D fp32 accumulator values: D / 8 per thread
+                float4* a = dq_acc + ((size_t)row * hq + h) * (D / 4) + sub * (D / 32);
+#pragma unroll
+                for (int j = 0; j < D / 32; ++j) a[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            d += __shfl_xor_sync(0xffffffffu, d, 1);
+            d += __shfl_xor_sync(0xffffffffu, d, 2);
+            d += __shfl_xor_sync(0xffffffffu, d, 4);
+            if (row < total_q && sub < 2) {
+                // record (row, h): two 16-byte halves, -LSE / scale (sub 0) and -D (sub 1)
+                const float l = (sub == 0 && row < rows) ? lse[(size_t)h * total_q + row] : 0.f;
+                rec[((size_t)row * hq + h) * 2 + sub] = split3_bf16(sub == 0 ? -l / scale : -d);
+                if (sub == 0 && sink && row < rows) {
+                    // probability mass on the sink, e^{sink - LSE}
+                    float ps;
+                    if (sg == -INFINITY)
+                        ps = 0.f;
+                    else if (l == INFINITY)
+                        ps = 1.f;
+                    else
+                        ps = __expf(sg - l);
+                    acc_sink += -ps * d;
+                }
             }
         }
-        d += __shfl_xor_sync(0xffffffffu, d, 1);
-        d += __shfl_xor_sync(0xffffffffu, d, 2);
-        d += __shfl_xor_sync(0xffffffffu, d, 4);
-        if (row < total_q && sub < 2) {
-            // record (row, h): two 16-byte halves, -LSE / scale (sub 0) and -D (sub 1)
-            const float l = (sub == 0 && row < rows) ? lse[(size_t)h * total_q + row] : 0.f;
-            rec[((size_t)row * hq + h) * 2 + sub] = split3_bf16(sub == 0 ? -l / scale : -d);
-            if (sub == 0 && sink && row < rows) {
-                // probability mass on the sink, e^{sink - LSE}
-                float ps;
-                if (sg == -INFINITY)
-                    ps = 0.f;
-                else if (l == INFINITY)
-                    ps = 1.f;
-                else
-                    ps = __expf(sg - l);
-                acc_sink += -ps * d;
-            }
+    }
+    if (kv_zero) {
+        // dK / dV rows cu_k[batch] .. total_k - 1 belong to no request and no
+        // CTA of the main kernel writes them.
+        const int k0 = min(total_k, max(0, cu_k[batch]));
+        const size_t n16 = (size_t)(total_k - k0) * hkv * (D / 8);
+        const size_t first = (size_t)k0 * hkv * (D / 8);
+        const size_t nthreads = (size_t)gridDim.x * gridDim.y * blockDim.x;
+        for (size_t i = ((size_t)blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + tid; i < n16; i += nthreads) {
+            dk[first + i] = make_uint4(0u, 0u, 0u, 0u);
+            dv[first + i] = make_uint4(0u, 0u, 0u, 0u);
         }
     }
     if (!sink) return;
@@ -1338,22 +1402,24 @@ static cudaError_t launch_d(const Args& a, void* workspace, cudaStream_t s, std:
         return e;
     }
     // dK/dV rows of keys no CTA visits (past every request's end) are zero
-    // (contiguous outputs only: a strided output shares its rows with other tensors).
+    // (contiguous outputs only: a strided output shares its rows with other
+    // tensors); the preprocess kernel clears them, or a memset when it does
+    // not run.
     const bool dkv_contig = a.dk_rs <= 0 && a.dv_rs <= 0;
-    if (dkv_contig && ((e = cudaMemsetAsync(a.dk, 0, (size_t)a.total_k * a.hkv * D * 2, s)) != cudaSuccess ||
-                       (e = cudaMemsetAsync(a.dv, 0, (size_t)a.total_k * a.hkv * D * 2, s)) != cudaSuccess)) {
+    if (a.total_q == 0 && dkv_contig && a.total_k > 0 &&
+        ((e = cudaMemsetAsync(a.dk, 0, (size_t)a.total_k * a.hkv * D * 2, s)) != cudaSuccess ||
+         (e = cudaMemsetAsync(a.dv, 0, (size_t)a.total_k * a.hkv * D * 2, s)) != cudaSuccess)) {
         *what = "memset dk/dv";
         return e;
     }
     if (a.total_q > 0) {
-        if ((e = cudaMemsetAsync(dq_accum, 0, acc_bytes, s)) != cudaSuccess) {
-            *what = "memset dq accumulator";
-            return e;
-        }
-        dim3 g1((a.total_q + 63) / 64, a.hq);
-        bwd_preprocess_kernel<D><<<g1, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(a.out),
-                                                 reinterpret_cast<const __nv_bfloat16*>(a.dout), a.lse, a.sink,
-                                                 rec, a.dsink, a.total_q, a.hq, a.scale, a.cu_q, a.batch);
+        const int n_rb = (a.total_q + 63) / 64;
+        dim3 g1(a.hq, n_rb < 65535 ? n_rb : 65535);
+        bwd_preprocess_kernel<D><<<g1, 256, 0, s>>>(
+            reinterpret_cast<const __nv_bfloat16*>(a.out), reinterpret_cast<const __nv_bfloat16*>(a.dout), a.lse,
+            a.sink, rec, a.dsink, reinterpret_cast<float4*>(dq_accum), a.total_q, a.hq, a.scale, a.cu_q, a.cu_k,
+            a.batch, reinterpret_cast<uint4*>(a.dk), reinterpret_cast<uint4*>(a.dv), a.total_k, a.hkv,
+            dkv_contig ? 1 : 0);
         if ((e = cudaGetLastError()) != cudaSuccess) {
             *what = "preprocess launch";
             return e;
@@ -1386,7 +1452,14 @@ static cudaError_t launch_d(const Args& a, void* workspace, cudaStream_t s, std:
         p.causal = a.causal;
         p.scale = a.scale;
         p.scale_log2 = a.scale * ATTN_LOG2E;
-        dim3 g2(a.hkv, a.batch, (a.max_seqlen_k + BN - 1) / BN);
+        p.batch = a.batch;
+        p.n_kt = (a.max_seqlen_k + BN - 1) / BN;
+        const long long n_cta = (long long)a.hkv * a.batch * p.n_kt;
+        if (n_cta > 0x7fffffffLL) {
+            *what = "too many key tiles for one launch";
+            return cudaErrorInvalidValue;
+        }
+        dim3 g2((unsigned)n_cta);
         if constexpr (D == 128) {
             const size_t smem = sizeof(d128::Smem) + 1024;
             static_assert(sizeof(d128::Smem) + 1024 <= 227 * 1024, "shared memory of the d 128 main kernel");

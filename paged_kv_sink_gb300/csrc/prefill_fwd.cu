@@ -117,7 +117,10 @@ __device__ __forceinline__ void tma_tile(uint8_t* dst, const CUtensorMap* m, uin
     for (int a = 0; a < Cfg<D>::kAtoms; ++a) tma_load_3d(dst + a * kAtom, m, bar, 64 * a, head, row);
 }
 
-template <int D>
+// kPaged: launched with a page table (the paged instantiation issues a tile's
+// page-segment copies from parallel lanes; the contiguous one never runs that
+// branch).
+template <int D, bool kPaged>
 __global__ void __launch_bounds__(kThreads, 2)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -263,10 +266,19 @@ __global__ void __launch_bounds__(kThreads, 2)
                             raise_status(ATTN_SINK_DEV_PAGE_OOB);
                     }
                     if (lane == 0) mbar_expect_tx(bar, kTile);
-                    for (int sg = 0; sg < nseg; ++sg) {
-                        const int sl = __shfl_sync(0xffffffffu, slot, sg);
-                        if (lane == 0)
-                            tma_tile<D>(dst0 + st * kTile + ((uint32_t)sg << p.seg_shift) * 128u, tm, bar, kvh, sl);
+                    if constexpr (kPaged) {
+                        // lane i issues the copy of segment i
+                        __syncwarp();
+                        if (lane < nseg)
+                            tma_tile<D>(dst0 + st * kTile + ((uint32_t)lane << p.seg_shift) * 128u, tm, bar, kvh,
+                                        slot);
+                    } else {
+                        for (int sg = 0; sg < nseg; ++sg) {
+                            const int sl = __shfl_sync(0xffffffffu, slot, sg);
+                            if (lane == 0)
+                                tma_tile<D>(dst0 + st * kTile + ((uint32_t)sg << p.seg_shift) * 128u, tm, bar, kvh,
+                                            sl);
+                        }
                     }
                 }
                 if (tail) {
@@ -641,13 +653,14 @@ static cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s, std::string* w
     p.causal = a.causal;
     p.scale_log2 = a.scale * ATTN_LOG2E;
     const size_t smem = sizeof(Smem<D>) + (Cfg<D>::kTwoPerSm ? 0 : 1024);
-    e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kernel = paged ? fwd_kernel<D, true> : fwd_kernel<D, false>;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) {
         *what = "smem attribute";
         return e;
     }
     dim3 grid(a.hq, p.n_rt, a.batch);
-    fwd_kernel<D><<<grid, kThreads, smem, s>>>(tq, tk, tv, p);
+    kernel<<<grid, kThreads, smem, s>>>(tq, tk, tv, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) *what = "launch";
     return e;

@@ -144,3 +144,36 @@ def test_bwd_neighbour_rows_do_not_leak(ext):
         assert not dq1[ql:qh].isnan().any() and not dk1[kl:kh].isnan().any() and not dv1[kl:kh].isnan().any()
         assert torch.equal(dk0[kl:kh], dk1[kl:kh]) and torch.equal(dv0[kl:kh], dv1[kl:kh])
         assert _rel(dq1[ql:qh], dq0[ql:qh]) <= 1e-5
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_rows_past_last_request_are_zero(ext, d):
+    """q / dout and k / v carry rows past the last request's (cu_seqlens[batch] <
+    total): into output buffers that hold NaN, the backward writes zeros there
+    (dq, and dk / dv with contiguous rows), and the requests' own gradients
+    equal those of the buffers without the extra rows."""
+    p = wl.make_prefill(seqlens_q=[100, 77], seqlens_k=[300, 129], hq=8, hkv=2, d=d, sink="normal",
+                        with_dout=True, seed=37)
+    dev = "cuda"
+    nq, nk = p.q.shape[0], p.k.shape[0]
+    ref = _fwd_bwd(ext, p.q, p.k, p.v, p.dout, p)
+
+    def pad(x, n):
+        return torch.cat([x, torch.randn((n,) + tuple(x.shape[1:])).to(x.dtype)])
+    q, dout = pad(p.q, 40).to(dev), pad(p.dout, 40).to(dev)
+    k, v = pad(p.k, 150).to(dev), pad(p.v, 150).to(dev)
+    sink = p.sink.to(dev)
+    cq, ck = p.cu_seqlens_q.to(dev), p.cu_seqlens_k.to(dev)
+    out, lse = ext.attn_sink_fwd(q, k, v, sink, cq, ck, p.max_seqlen_q, p.max_seqlen_k)
+    dq = torch.full_like(q, float("nan"))
+    dk, dv = torch.full_like(k, float("nan")), torch.full_like(v, float("nan"))
+    _, _, _, ds = ext.attn_sink_bwd(q, k, v, sink, out, lse, dout, cq, ck, p.max_seqlen_q, p.max_seqlen_k,
+                                    dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    assert ext.device_status() == 0
+    dq, dk, dv, ds = dq.cpu(), dk.cpu(), dv.cpu(), ds.cpu()
+    assert torch.count_nonzero(dq[nq:]) == 0 and not dq[nq:].isnan().any()
+    for x in (dk, dv):
+        assert torch.count_nonzero(x[nk:]) == 0 and not x[nk:].isnan().any()
+    assert torch.equal(dk[:nk], ref[1]) and torch.equal(dv[:nk], ref[2])
+    assert _rel(dq[:nq], ref[0]) <= 1e-5 and _rel(ds, ref[3]) <= 1e-5
