@@ -39,16 +39,16 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # Keyed by kernel + workload; each entry records the hash of the kernel source
 # it was measured on and is reported only while that source is unchanged.
 NCU_TRAFFIC = {
-    # fwd_kernel<64>: 442.5 MB read + 259.7 MB written per launch
-    "fwd_kernel/extend_varlen": {"src": "be9e0f6a91f4c9cf", "bytes": 702_200_576},
-    # fwd_kernel<64>, first 1024 + last 7168 window: 489.5 MB + 268.2 MB
-    "fwd_kernel/extend_window": {"src": "be9e0f6a91f4c9cf", "bytes": 757_656_320},
-    # fwd_kernel<64> reading K/V through a page-16 table: 448.7 MB + 259.3 MB
-    "fwd_kernel/extend_paged": {"src": "be9e0f6a91f4c9cf", "bytes": 707_991_552},
-    # bwd_main_kernel<64>: 2.748 GB read + 1.058 GB written per launch
-    "bwd_main_kernel/train": {"src": "76296cbf95b92602", "bytes": 3_806_221_568},
-    # bwd_main128_kernel on the head-dim-128 training step: 2.676 GB + 1.217 GB
-    "bwd_main128_kernel/train_d128": {"src": "76296cbf95b92602", "bytes": 3_892_545_280},
+    # fwd_kernel<64>: 442.5 MB read + 258.7 MB written per launch
+    "fwd_kernel/extend_varlen": {"src": "7529f71a2f0dda75", "bytes": 701_152_768},
+    # fwd_kernel<64>, first 1024 + last 7168 window: 489.4 MB + 268.3 MB
+    "fwd_kernel/extend_window": {"src": "7529f71a2f0dda75", "bytes": 757_739_008},
+    # fwd_kernel<64> reading K/V through a page-16 table: 445.9 MB + 258.8 MB
+    "fwd_kernel/extend_paged": {"src": "7529f71a2f0dda75", "bytes": 704_646_400},
+    # bwd_main_kernel<64>: 2.690 GB read + 1.046 GB written per launch
+    "bwd_main_kernel/train": {"src": "b8fb4872ca07bcb0", "bytes": 3_735_658_496},
+    # bwd_main128_kernel on the head-dim-128 training step: 1.930 GB + 0.960 GB
+    "bwd_main128_kernel/train_d128": {"src": "b8fb4872ca07bcb0", "bytes": 2_890_048_768},
     # decode_split_kernel: 1.943 GB + 0.011 GB
     "decode/decode_sink": {"src": "c0d40bc40087f07f", "bytes": 1_954_153_216},
     # decode_split_kernel: 1.074 GB + 0.007 GB
