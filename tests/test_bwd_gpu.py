@@ -56,6 +56,9 @@ CASES = {
     # the sglang window (first 1024 + last 7168) past 8192 keys: the key tiles in the
     # gap between the windows see no query row, a first window wider than a tile
     "window_1024_7168": ([384], [9000], 2, 1, (-2.0, 4.0), 1024, 7168, True),
+    # more than 32 key tiles in several (KV head, request) groups: the head-dim-128
+    # kernel launches its key tiles in bands of 16, the head-dim-64 one tile-major
+    "banded_groups": ([300, 4100], [5000, 4200], 4, 2, "normal", 0, 0, True),
 }
 
 
@@ -75,9 +78,9 @@ def test_bwd_matches_oracle(ext, name):
         assert_grad_close(ds, rs, f"{name} dsink")
 
 
-# head_dim 128: the main kernel runs in two passes of 64 output columns each.
+# head_dim 128 (bwd_main128_kernel: 64-query steps, dQ^T with the head dims on the TMEM lanes).
 D128_CASES = ["square_gqa2", "ragged_extend", "mha", "no_sink", "non_causal", "window_small", "more_q_than_k",
-              "window_1024_7168"]
+              "window_1024_7168", "banded_groups"]
 
 
 @pytest.mark.parametrize("name", D128_CASES)
