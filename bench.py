@@ -45,10 +45,10 @@ NCU_TRAFFIC = {
     "fwd_kernel/extend_window": {"src": "7529f71a2f0dda75", "bytes": 757_739_008},
     # fwd_kernel<64> reading K/V through a page-16 table: 445.9 MB + 258.8 MB
     "fwd_kernel/extend_paged": {"src": "7529f71a2f0dda75", "bytes": 704_646_400},
-    # bwd_main_kernel<64>: 2.690 GB read + 1.046 GB written per launch
-    "bwd_main_kernel/train": {"src": "b8fb4872ca07bcb0", "bytes": 3_735_658_496},
-    # bwd_main128_kernel on the head-dim-128 training step: 1.930 GB + 0.960 GB
-    "bwd_main128_kernel/train_d128": {"src": "b8fb4872ca07bcb0", "bytes": 2_890_048_768},
+    # bwd_main_kernel<64>: 2.684 GB read + 1.048 GB written per launch
+    "bwd_main_kernel/train": {"src": "8450e18315e5943f", "bytes": 3_731_941_632},
+    # bwd_main128_kernel on the head-dim-128 training step: 1.910 GB + 0.946 GB
+    "bwd_main128_kernel/train_d128": {"src": "8450e18315e5943f", "bytes": 2_856_080_128},
     # decode_split_kernel: 1.943 GB + 0.011 GB
     "decode/decode_sink": {"src": "c0d40bc40087f07f", "bytes": 1_954_153_216},
     # decode_split_kernel: 1.074 GB + 0.007 GB

@@ -964,6 +964,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     umma_commit_e(&S.s_full);
                     // P^T of the previous step sits in the dP^T columns until dV has read it
                     if (t > 0 && !(ok = mbar_wait_warp(&S.pv_done, (t - 1) & 1, abort))) break;
+                    // and once dK / dQ^T of the previous step are done: the elementwise warps
+                    // then learn that from dp_full (no wait of their own before they write
+                    // dS^T / dS over it).  Measured 1 % faster here, 3 % slower at d 64.
+                    if (t > 0 && !(ok = mbar_wait_warp(&S.mma2_done, (t - 1) & 1, abort))) break;
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
@@ -1108,10 +1112,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else
                     ds_cols<true, 0>(pa, dr, lo, hi, dw);
             }
-            if (t > 0) {  // dK and dQ^T of the previous step are done with dS^T and dS
-                if (!(ok = mbar_wait_warp(&S.mma2_done, (t - 1) & 1, abort))) break;
-                tc_fence_after();
-            }
+            // dK and dQ^T of the previous step are done with dS^T and dS: dP^T of this step
+            // (waited above) was issued after them.
             tmem_st16(tmem + lane_base + cDS + 16 * hh, dw);  // dS^T: the A of dK
             // dS row r, queries 32 hh .. 32 hh + 31 = 16-byte chunks 4 hh .. 4 hh + 3: the B of dQ^T
 #pragma unroll
