@@ -201,6 +201,28 @@ __global__ void __launch_bounds__(kThreads, 2)
         mbar_init(&S.v_tail, 1);
         S.abort = 0;
         fence_mbar_init();
+        // Contiguous K / V: Q and the first ring's worth of K and V tiles are
+        // requested now, so they load while TMEM is allocated and the CTA
+        // synchronises (about a third of a CTA's fixed start-up time); the
+        // producer warps take over from the next tile on.
+        if constexpr (!kPaged) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            mbar_expect_tx(&S.q_full, kTile);
+            tma_tile<D>(S.q, &tm_q, &S.q_full, h, q_start + qs);
+            for (int it = 0; it < ntiles && it < KSTAGE; ++it) {
+                const int t = it < ta ? it : tb + (it - ta);
+                mbar_expect_tx(&S.k_full[it], kTile);
+                tma_tile<D>(S.k[it], &tm_k, &S.k_full[it], kvh, k_start + t * BN);
+            }
+            for (int it = 0; it < ntiles && it < VSTAGE; ++it) {
+                const int t = it < ta ? it : tb + (it - ta);
+                uint64_t* bar = (t + 1) * BN > Lk ? &S.v_tail : &S.v_full[it];
+                mbar_expect_tx(bar, kTile);
+                tma_tile<D>(S.v[it], &tm_v, bar, kvh, k_start + t * BN);
+            }
+        }
     }
     if (warp == 1) {
         tmem_alloc(&S.tmem_base, C::kTmemCols);
@@ -226,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             uint8_t* dst0 = is_k ? S.k[0] : S.v[0];
             const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
             const int nseg = BN >> p.seg_shift;
-            if (lane == 0) {
+            if (paged && lane == 0) {
                 prefetch_tmap(tm);
                 if (is_k) {
                     prefetch_tmap(&tm_q);
@@ -249,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const bool tail = !is_k && (t + 1) * BN > Lk;
                 uint64_t* bar = tail ? &S.v_tail : &full[st];
                 if (!paged) {
-                    if (lane == 0) {
+                    if (lane == 0 && it >= nst) {  // the first nst were issued at start-up
                         mbar_expect_tx(bar, kTile);
                         tma_tile<D>(dst0 + st * kTile, tm, bar, kvh, k_start + t * BN);
                     }
