@@ -39,12 +39,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # Keyed by kernel + workload; each entry records the hash of the kernel source
 # it was measured on and is reported only while that source is unchanged.
 NCU_TRAFFIC = {
-    # fwd_kernel<64>: 442.5 MB read + 258.7 MB written per launch
-    "fwd_kernel/extend_varlen": {"src": "7529f71a2f0dda75", "bytes": 701_152_768},
-    # fwd_kernel<64>, first 1024 + last 7168 window: 489.4 MB + 268.3 MB
-    "fwd_kernel/extend_window": {"src": "7529f71a2f0dda75", "bytes": 757_739_008},
-    # fwd_kernel<64> reading K/V through a page-16 table: 445.9 MB + 258.8 MB
-    "fwd_kernel/extend_paged": {"src": "7529f71a2f0dda75", "bytes": 704_646_400},
+    # fwd_kernel<64>: 442.7 MB read + 259.0 MB written per launch
+    "fwd_kernel/extend_varlen": {"src": "078791a9929e5a67", "bytes": 701_718_272},
+    # fwd_kernel<64>, first 1024 + last 7168 window: 489.3 MB + 268.3 MB
+    "fwd_kernel/extend_window": {"src": "078791a9929e5a67", "bytes": 757_571_072},
+    # fwd_kernel<64> reading K/V through a page-16 table: 445.7 MB + 258.9 MB
+    "fwd_kernel/extend_paged": {"src": "078791a9929e5a67", "bytes": 704_532_992},
     # bwd_main_kernel<64>: 2.684 GB read + 1.048 GB written per launch
     "bwd_main_kernel/train": {"src": "8450e18315e5943f", "bytes": 3_731_941_632},
     # bwd_main128_kernel on the head-dim-128 training step: 1.910 GB + 0.946 GB
