@@ -611,12 +611,16 @@ __global__ void __launch_bounds__(kThreads, 2)
 // S, which a single 128-row tile per SM leaves idle.
 namespace x2 {
 constexpr int kThreads = 384;   // warps 0-3 control, 4-7 softmax A, 8-11 softmax B
-constexpr int kStages = 2;      // K and V rings
 constexpr int kRegsCtrl = 72;   // 128 * 72 + 256 * 216 = 64512 = 384 * 168 (launch)
 constexpr int kRegsSoftmax = 216;
-constexpr uint32_t kTile = 2 * kAtom;  // 128 rows x 128 head dims
+// K / V ring stages: 2 at head dim 128 (192 KB in all with the two Q tiles).
+template <int D>
+constexpr int kStagesFor = D == 64 ? 3 : 2;
 
+template <int D>
 struct __align__(1024) Smem {
+    static constexpr int kStages = kStagesFor<D>;
+    static constexpr uint32_t kTile = Cfg<D>::kTile;
     uint8_t q[2][kTile];
     uint8_t k[kStages][kTile];
     uint8_t v[kStages][kTile];
@@ -631,18 +635,17 @@ struct __align__(1024) Smem {
 };
 }  // namespace x2
 
-template <bool kPaged>
+template <int D, bool kPaged>
 __global__ void __launch_bounds__(x2::kThreads, 1)
     fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const Params p) {
-    constexpr int D = 128;
     using C = Cfg<D>;
-    using x2::kStages;
-    constexpr uint32_t kTile = x2::kTile;
+    constexpr int kStages = x2::kStagesFor<D>;
+    constexpr uint32_t kTile = C::kTile;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem_al =
         reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    x2::Smem& S = *reinterpret_cast<x2::Smem*>(smem_al);
+    x2::Smem<D>& S = *reinterpret_cast<x2::Smem<D>*>(smem_al);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Grid (head pair, row tile, request), as fwd_kernel with head pairs.
@@ -1098,8 +1101,16 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int d, int heads, long lo
     return cudaSuccess;
 }
 
+// Head dim 128 runs two query heads per CTA (fwd2_kernel) when the group is even.
+// At head dim 64 the same kernel measured 833 against 1158 TFLOP/s on the varlen
+// extend: there two independent CTAs per SM (fwd_kernel) keep the tensor core
+// busier than one CTA whose two chains wait for each P V before the next S.
+template <int D>
+constexpr bool kTwoHeadsFor = D == 128;
+
 template <int D>
 static cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s, std::string* what) {
+    constexpr bool kTwoHeads = kTwoHeadsFor<D>;
     CUtensorMap tq, tk, tv;
     cudaError_t e;
     const bool paged = a.page_table != nullptr;
@@ -1134,11 +1145,11 @@ static cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s, std::string* w
     p.causal = a.causal;
     p.scale_log2 = a.scale * ATTN_LOG2E;
     const size_t smem = sizeof(Smem<D>) + (Cfg<D>::kTwoPerSm ? 0 : 1024);
-    if (D == 128 && p.group % 2 == 0) {
-        // head dim 128 with an even query-head group: two heads per CTA (fwd2_kernel)
-        const size_t smem2 = sizeof(x2::Smem) + 1024;
-        static_assert(sizeof(x2::Smem) + 1024 <= 227 * 1024, "shared memory of fwd2_kernel");
-        auto kernel2 = paged ? fwd2_kernel<true> : fwd2_kernel<false>;
+    if constexpr (kTwoHeads) if (p.group % 2 == 0) {
+        // an even query-head group: two heads per CTA (fwd2_kernel)
+        const size_t smem2 = sizeof(x2::Smem<D>) + 1024;
+        static_assert(sizeof(x2::Smem<D>) + 1024 <= 227 * 1024, "shared memory of fwd2_kernel");
+        auto kernel2 = paged ? fwd2_kernel<D, true> : fwd2_kernel<D, false>;
         e = cudaFuncSetAttribute(kernel2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
         if (e != cudaSuccess) {
             *what = "smem attribute";
