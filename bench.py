@@ -39,12 +39,14 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # Keyed by kernel + workload; each entry records the hash of the kernel source
 # it was measured on and is reported only while that source is unchanged.
 NCU_TRAFFIC = {
-    # fwd_kernel<64>: 442.7 MB read + 259.0 MB written per launch
-    "fwd_kernel/extend_varlen": {"src": "078791a9929e5a67", "bytes": 701_718_272},
-    # fwd_kernel<64>, first 1024 + last 7168 window: 489.3 MB + 268.3 MB
-    "fwd_kernel/extend_window": {"src": "078791a9929e5a67", "bytes": 757_571_072},
-    # fwd_kernel<64> reading K/V through a page-16 table: 445.7 MB + 258.9 MB
-    "fwd_kernel/extend_paged": {"src": "078791a9929e5a67", "bytes": 704_532_992},
+    # fwd_kernel<64>: 442.6 MB read + 259.1 MB written per launch
+    "fwd_kernel/extend_varlen": {"src": "8b443d22c5cc1afe", "bytes": 701_665_536},
+    # fwd_kernel<64>, first 1024 + last 7168 window: 488.2 MB + 267.8 MB
+    "fwd_kernel/extend_window": {"src": "8b443d22c5cc1afe", "bytes": 756_048_384},
+    # fwd_kernel<64> reading K/V through a page-16 table: 445.7 MB + 258.7 MB
+    "fwd_kernel/extend_paged": {"src": "8b443d22c5cc1afe", "bytes": 704_348_672},
+    # fwd2_kernel<128> (two query heads per CTA): 1010.0 MB + 273.3 MB
+    "fwd_kernel/extend_d128": {"src": "8b443d22c5cc1afe", "bytes": 1_283_301_632},
     # bwd_main_kernel<64>: 2.684 GB read + 1.048 GB written per launch
     "bwd_main_kernel/train": {"src": "8450e18315e5943f", "bytes": 3_731_941_632},
     # bwd_main128_kernel on the head-dim-128 training step: 1.910 GB + 0.946 GB
@@ -259,7 +261,8 @@ def bench_extend(torch, ext, dev, p, steps, warmup, flush, peaks, peak_src, sync
     flops = fwd_flops(p)  # visible (query, key) pairs only: keys a window skips are work avoided
     ms = sum(times) / len(times)
     achieved = flops / (ms * 1e-3) / 1e12
-    roof = {"kernel": "attn::prefill::fwd_kernel", "bound": "tensor", "achieved": achieved,
+    kname = "attn::prefill::fwd2_kernel" if p.head_dim == 128 and (p.hq // p.hkv) % 2 == 0 else "attn::prefill::fwd_kernel"
+    roof = {"kernel": kname, "bound": "tensor", "achieved": achieved,
             "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
             "peak_source": f"bf16 burst, {peak_src}",
             "traffic": _traffic("fwd_kernel/" + p.name.split()[0], "prefill_fwd.cu"),
