@@ -118,6 +118,20 @@ def test_train_full_size_sampled(ext):
     assert_grad_close(ds[:8], rs[:8], "dsink")
 
 
+@pytest.mark.slow
+def test_train_d128_full_size_sampled(ext):
+    """Head-dim-128 training workload at full size (B 2, L 8192, Hq 32, Hkv 8; the
+    key tiles launched in bands): dK/dV of KV head 0, dQ of its four query heads
+    and their dsink, both requests."""
+    p = wl.workload("train_d128")
+    dq, dk, dv, ds = run_fwd_bwd(ext, p)
+    rq, rk, rv, rs, _, _ = oracle_bwd(p, kv_heads=[0], check_identity=False)
+    assert_grad_close(dq[:, :4], rq[:, :4], "dq")
+    assert_grad_close(dk[:, :1], rk[:, :1], "dk")
+    assert_grad_close(dv[:, :1], rv[:, :1], "dv")
+    assert_grad_close(ds[:4], rs[:4], "dsink")
+
+
 def test_train_step_cuda_graph_replay(ext):
     """Forward + backward captured once in a CUDA graph (the backward's scratch
     comes from the stream-ordered pool inside the capture) and replayed on new

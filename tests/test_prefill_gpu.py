@@ -124,10 +124,12 @@ def _sample_rows(p, per_req, seed=0):
     return rows
 
 
-@pytest.mark.parametrize("name", ["prefill_tiny", "extend_varlen", "extend_window", "train"])
+@pytest.mark.parametrize("name", ["prefill_tiny", "extend_varlen", "extend_window", "train", "extend_d128",
+                                  "train_d128"])
 def test_full_size_workloads_sampled(ext, name):
     """The named workloads at full size in the bench's launch configuration;
-    sampled rows (all heads) against the oracle, the tiny one completely."""
+    sampled rows (all heads) against the oracle, the tiny one completely.  The
+    head-dim-128 ones run two query heads per CTA (fwd2_kernel)."""
     p = wl.workload(name)
     out, lse = run_fwd(ext, p)
     if name == "prefill_tiny":
