@@ -24,3 +24,8 @@ from ._lib import (  # noqa: F401
     device_status,
     lib,
 )
+from .autograd import (  # noqa: F401
+    attn_sink_func,
+    attn_sink_varlen_func,
+    attn_sink_varlen_qkvpacked_func,
+)

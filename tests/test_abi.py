@@ -133,3 +133,21 @@ def test_validation_of_the_extended_entry_points_without_gpu(lib):
     assert fwd_host([0, 5], [0, 5], 1, head_dim=96) == -2
     assert fwd_host([0], [0], 0) == 0
     assert fwd_host([0, 0, 0], [0, 7, 9], 2) == 0  # no query rows: nothing to do
+
+
+def test_autograd_functions_check_arguments_on_the_host(lib):
+    """The autograd functions only marshal arguments: host tensors and
+    malformed shapes are rejected before any library call."""
+    import torch
+    import paged_kv_sink_gb300 as ext
+    q = torch.zeros(4, 2, 64, dtype=torch.bfloat16)
+    kv = torch.zeros(4, 1, 64, dtype=torch.bfloat16)
+    cu = torch.tensor([0, 4], dtype=torch.int32)
+    with pytest.raises(TypeError, match="CUDA"):
+        ext.attn_sink_varlen_func(q, kv, kv, cu, cu, 4, 4)
+    with pytest.raises(TypeError, match="batch, seqlen"):
+        ext.attn_sink_func(q, kv, kv)
+    with pytest.raises(TypeError, match="hkv"):
+        ext.attn_sink_varlen_qkvpacked_func(torch.zeros(4, 6, 64, dtype=torch.bfloat16), cu, 4)
+    with pytest.raises(TypeError, match="CUDA"):
+        ext.attn_sink_varlen_qkvpacked_func(torch.zeros(4, 3, 2, 64, dtype=torch.bfloat16), cu, 4)
