@@ -8,6 +8,7 @@ from ._lib import (  # noqa: F401
     EXPORTS,
     AttnSinkError,
     attn_sink_bwd,
+    attn_sink_bwd_kvpacked,
     attn_sink_bwd_qkvpacked,
     attn_sink_decode_paged,
     attn_sink_decode_paged_append,
@@ -26,6 +27,9 @@ from ._lib import (  # noqa: F401
 )
 from .autograd import (  # noqa: F401
     attn_sink_func,
+    attn_sink_kvpacked_func,
+    attn_sink_qkvpacked_func,
     attn_sink_varlen_func,
+    attn_sink_varlen_kvpacked_func,
     attn_sink_varlen_qkvpacked_func,
 )

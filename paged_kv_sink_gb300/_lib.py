@@ -280,6 +280,36 @@ def attn_sink_bwd_qkvpacked(qkv, hkv, sink, out, lse, dout, cu_seqlens_q, max_se
     return (dqkv.reshape(shape4) if shape4 is not None else dqkv), dsink
 
 
+def attn_sink_bwd_kvpacked(q, kv, sink, out, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
+                           max_seqlen_k, win_first=0, win_last=0, causal=True, scale=0.0, dq=None, dkv=None,
+                           dsink=None, stream=None):
+    """Backward of attn_sink_fwd_kvpacked; returns (dq, dkv, dsink or None), dkv in
+    the (Tk, 2, hkv, d) layout of kv.  Rows of dkv past every request's last key
+    are not written (pass a zeroed ``dkv`` if kv has such rows)."""
+    for t, n in ((q, "q"), (kv, "kv"), (out, "out"), (dout, "dout")):
+        _need(t, torch.bfloat16, n)
+    _need(sink, torch.float32, "sink")
+    _need(lse, torch.float32, "lse")
+    tq, hq, d = q.shape
+    tk, _, hkv, _ = kv.shape
+    dq = torch.empty_like(q) if dq is None else dq
+    dkv = torch.empty_like(kv) if dkv is None else dkv
+    _need(dkv, torch.bfloat16, "dkv")
+    if sink is not None and dsink is None:
+        dsink = torch.empty_like(sink)
+    kp, rs = _row_view(kv.reshape(tk, 2 * hkv, d), 0, hkv, d)
+    vp, _ = _row_view(kv.reshape(tk, 2 * hkv, d), hkv, hkv, d)
+    dkp, drs = _row_view(dkv.reshape(tk, 2 * hkv, d), 0, hkv, d)
+    dvp, _ = _row_view(dkv.reshape(tk, 2 * hkv, d), hkv, hkv, d)
+    rc = lib().attn_sink_bwd_strided(_ptr(q), kp, vp, 0, rs, rs, _ptr(sink), _ptr(out), _ptr(lse), _ptr(dout),
+                                     _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), cu_seqlens_q.numel() - 1, tq, tk, hq,
+                                     hkv, d, int(max_seqlen_q), int(max_seqlen_k), int(win_first),
+                                     int(win_last), 1 if causal else 0, float(scale), _ptr(dq), dkp, dvp, 0, drs,
+                                     drs, _ptr(dsink), _stream(stream))
+    _check("attn_sink_bwd_strided", rc)
+    return dq, dkv, dsink
+
+
 def attn_sink_kv_append(k_new, v_new, k_cache, v_cache, page_table, seqlens, cu_new=None,
                         max_new=None, stream=None):
     """Writes the new K/V rows into the paged caches in place (see the C header)."""

@@ -55,11 +55,36 @@ class _AttnSinkVarlenQKVPacked(torch.autograd.Function):
     def backward(ctx, dout, _dlse):
         qkv, sink, out, lse, cu = ctx.saved_tensors
         hkv, max_s, win_first, win_last, causal, scale = ctx.args
+        # zeroed: rows past the last sequence's end (padding) are not written
         dqkv, dsink = _lib.attn_sink_bwd_qkvpacked(qkv, hkv, sink, out, lse, dout.contiguous(), cu, max_s,
-                                                   win_first, win_last, causal, scale)
+                                                   win_first, win_last, causal, scale,
+                                                   dqkv=torch.zeros_like(qkv))
         if sink is None or not ctx.needs_input_grad[2]:
             dsink = None
         return dqkv, None, dsink, None, None, None, None, None, None
+
+
+class _AttnSinkVarlenKVPacked(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, kv, sink, cu_q, cu_k, max_q, max_k, causal, win_first, win_last, scale):
+        out, lse = _lib.attn_sink_fwd_kvpacked(q, kv, sink, cu_q, cu_k, max_q, max_k, win_first, win_last,
+                                               causal, scale)
+        ctx.save_for_backward(q, kv, sink, out, lse, cu_q, cu_k)
+        ctx.args = (max_q, max_k, win_first, win_last, causal, scale)
+        ctx.mark_non_differentiable(lse)
+        return out, lse
+
+    @staticmethod
+    def backward(ctx, dout, _dlse):
+        q, kv, sink, out, lse, cu_q, cu_k = ctx.saved_tensors
+        max_q, max_k, win_first, win_last, causal, scale = ctx.args
+        # zeroed: rows past the last sequence's end (padding) are not written
+        dq, dkv, dsink = _lib.attn_sink_bwd_kvpacked(q, kv, sink, out, lse, dout.contiguous(), cu_q, cu_k, max_q,
+                                                     max_k, win_first, win_last, causal, scale,
+                                                     dkv=torch.zeros_like(kv))
+        if sink is None or not ctx.needs_input_grad[2]:
+            dsink = None
+        return dq, dkv, dsink, None, None, None, None, None, None, None, None
 
 
 def attn_sink_varlen_func(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
@@ -84,9 +109,7 @@ def attn_sink_func(q, k, v, learnable_sink=None, causal=True, win_first=0, win_l
         raise TypeError("attn_sink_func takes (batch, seqlen, heads, head_dim) tensors")
     B, sq, hq, d = q.shape
     sk = k.shape[1]
-    dev = q.device
-    cu_q = torch.arange(0, (B + 1) * sq, sq, dtype=torch.int32, device=dev)
-    cu_k = torch.arange(0, (B + 1) * sk, sk, dtype=torch.int32, device=dev)
+    cu_q, cu_k = _cu(B, sq, q.device), _cu(B, sk, q.device)
     out, lse = _AttnSinkVarlen.apply(q.reshape(B * sq, hq, d), k.reshape(B * sk, k.shape[2], d),
                                      v.reshape(B * sk, v.shape[2], d), learnable_sink, cu_q, cu_k, sq, sk,
                                      bool(causal), int(win_first), int(win_last), _scale(softmax_scale))
@@ -107,4 +130,51 @@ def attn_sink_varlen_qkvpacked_func(qkv, cu_seqlens, max_seqlen, hkv=None, learn
         raise TypeError("hkv is required for a (total, Hq + 2 Hkv, head_dim) qkv")
     out, lse = _AttnSinkVarlenQKVPacked.apply(qkv, int(hkv), learnable_sink, cu_seqlens, int(max_seqlen),
                                               bool(causal), int(win_first), int(win_last), _scale(softmax_scale))
+    return (out, lse) if return_lse else out
+
+
+def attn_sink_varlen_kvpacked_func(q, kv, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                                   learnable_sink=None, causal=True, win_first=0, win_last=0, softmax_scale=None,
+                                   return_lse=False):
+    """q (total_q, Hq, d) against a packed kv (total_k, 2, Hkv, d); differentiable in
+    q, kv and ``learnable_sink``.  The gradient of kv comes back in its layout."""
+    if kv.dim() != 4 or kv.shape[1] != 2:
+        raise TypeError("kv must be (total_k, 2, heads, head_dim)")
+    out, lse = _AttnSinkVarlenKVPacked.apply(q, kv, learnable_sink, cu_seqlens_q, cu_seqlens_k, int(max_seqlen_q),
+                                             int(max_seqlen_k), bool(causal), int(win_first), int(win_last),
+                                             _scale(softmax_scale))
+    return (out, lse) if return_lse else out
+
+
+def _cu(batch, seqlen, device):
+    return torch.arange(0, (batch + 1) * seqlen, seqlen, dtype=torch.int32, device=device)
+
+
+def attn_sink_qkvpacked_func(qkv, learnable_sink=None, causal=True, win_first=0, win_last=0, softmax_scale=None,
+                             return_lse=False):
+    """Equal-length batches of packed self-attention: qkv (B, S, 3, H, d).
+    Returns out (B, S, H, d) (and LSE (H, B * S) when ``return_lse``)."""
+    if qkv.dim() != 5 or qkv.shape[2] != 3:
+        raise TypeError("qkv must be (batch, seqlen, 3, heads, head_dim)")
+    B, S, _, H, d = qkv.shape
+    out, lse = attn_sink_varlen_qkvpacked_func(qkv.reshape(B * S, 3, H, d), _cu(B, S, qkv.device), S,
+                                               learnable_sink=learnable_sink, causal=causal, win_first=win_first,
+                                               win_last=win_last, softmax_scale=softmax_scale, return_lse=True)
+    out = out.reshape(B, S, H, d)
+    return (out, lse) if return_lse else out
+
+
+def attn_sink_kvpacked_func(q, kv, learnable_sink=None, causal=True, win_first=0, win_last=0, softmax_scale=None,
+                            return_lse=False):
+    """Equal-length batches: q (B, Sq, Hq, d) against kv (B, Sk, 2, Hkv, d).
+    Returns out (B, Sq, Hq, d) (and LSE (Hq, B * Sq) when ``return_lse``)."""
+    if q.dim() != 4 or kv.dim() != 5 or kv.shape[2] != 2:
+        raise TypeError("q must be (batch, seqlen, heads, head_dim) and kv (batch, seqlen, 2, heads, head_dim)")
+    B, sq, hq, d = q.shape
+    sk, hkv = kv.shape[1], kv.shape[3]
+    out, lse = attn_sink_varlen_kvpacked_func(q.reshape(B * sq, hq, d), kv.reshape(B * sk, 2, hkv, d),
+                                              _cu(B, sq, q.device), _cu(B, sk, q.device), sq, sk,
+                                              learnable_sink=learnable_sink, causal=causal, win_first=win_first,
+                                              win_last=win_last, softmax_scale=softmax_scale, return_lse=True)
+    out = out.reshape(B, sq, hq, d)
     return (out, lse) if return_lse else out

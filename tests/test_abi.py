@@ -151,3 +151,9 @@ def test_autograd_functions_check_arguments_on_the_host(lib):
         ext.attn_sink_varlen_qkvpacked_func(torch.zeros(4, 6, 64, dtype=torch.bfloat16), cu, 4)
     with pytest.raises(TypeError, match="CUDA"):
         ext.attn_sink_varlen_qkvpacked_func(torch.zeros(4, 3, 2, 64, dtype=torch.bfloat16), cu, 4)
+    with pytest.raises(TypeError, match="kv must be"):
+        ext.attn_sink_varlen_kvpacked_func(q, kv, cu, cu, 4, 4)
+    with pytest.raises(TypeError, match="qkv must be"):
+        ext.attn_sink_qkvpacked_func(torch.zeros(4, 3, 2, 64, dtype=torch.bfloat16))
+    with pytest.raises(TypeError, match="CUDA"):
+        ext.attn_sink_kvpacked_func(q.reshape(1, 4, 2, 64), torch.zeros(1, 4, 2, 1, 64, dtype=torch.bfloat16))

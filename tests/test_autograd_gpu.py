@@ -143,3 +143,75 @@ def test_sink_trains(ext):
     assert all(b < a for a, b in zip(losses, losses[1:])), losses
     assert losses[-1] < 0.9 * losses[0], losses
     assert bool((s.detach() > s0).all()), (s0, s.detach())
+
+
+def test_varlen_kvpacked_func_gradients(ext):
+    p = wl.make_prefill(seqlens_q=[100, 257], seqlens_k=[300, 400], hq=8, hkv=2, d=64, sink="normal",
+                        with_dout=True, seed=61)
+    q = _leaf(p.q)
+    kv = _leaf(torch.stack([p.k, p.v], dim=1).contiguous())  # (Tk, 2, Hkv, d)
+    s = _leaf(p.sink)
+    cq, ck = p.cu_seqlens_q.cuda(), p.cu_seqlens_k.cuda()
+    out = ext.attn_sink_varlen_kvpacked_func(q, kv, cq, ck, p.max_seqlen_q, p.max_seqlen_k, learnable_sink=s)
+    out.backward(p.dout.cuda())
+    torch.cuda.synchronize()
+    assert ext.device_status() == 0
+    assert kv.grad.shape == kv.shape
+    rq, rk, rv, rs, ro, _ = _oracle(p)
+    assert_out_close(out.detach().cpu(), ro, "out")
+    assert_grad_close(q.grad.cpu(), rq, "dq")
+    assert_grad_close(kv.grad[:, 0].cpu(), rk, "dk")
+    assert_grad_close(kv.grad[:, 1].cpu(), rv, "dv")
+    assert_grad_close(s.grad.cpu(), rs, "dsink")
+
+
+def test_fixed_length_packed_forms_equal_varlen(ext):
+    """(B, S, 3, H, d) and (B, Sk, 2, Hkv, d) batches give the varlen packed
+    functions' results; padding rows past the last sequence get zero gradient."""
+    g = torch.Generator().manual_seed(7)
+    B, S, H, d = 2, 140, 4, 64
+    qkv0 = torch.randn(B, S, 3, H, d, generator=g).to(torch.bfloat16)
+    s0 = torch.randn(H, generator=g, dtype=torch.float32)
+    do = torch.randn(B, S, H, d, generator=g).to(torch.bfloat16).cuda()
+    qkv, s = _leaf(qkv0), _leaf(s0)
+    out = ext.attn_sink_qkvpacked_func(qkv, learnable_sink=s)
+    out.backward(do)
+    # the same sequences inside a buffer with 5 padding rows at the end
+    pad = torch.randn(5, 3, H, d, generator=g).to(torch.bfloat16)
+    qkv2 = _leaf(torch.cat([qkv0.reshape(B * S, 3, H, d), pad]))
+    s2 = _leaf(s0)
+    cu = torch.arange(0, (B + 1) * S, S, dtype=torch.int32, device="cuda")
+    out2 = ext.attn_sink_varlen_qkvpacked_func(qkv2, cu, S, learnable_sink=s2)
+    out2[:B * S].backward(do.reshape(B * S, H, d))
+    torch.cuda.synchronize()
+    assert ext.device_status() == 0
+    assert torch.equal(out.detach().reshape(B * S, H, d), out2.detach()[:B * S])
+    g1 = qkv.grad.reshape(B * S, 3, H, d)
+    assert torch.equal(g1[:, 1:], qkv2.grad[:B * S, 1:])  # dK, dV: fixed accumulation order
+    assert rel_fro(g1[:, 0].cpu(), qkv2.grad[:B * S, 0].cpu()) < 1e-5
+    assert torch.count_nonzero(qkv2.grad[B * S:]) == 0
+    assert rel_fro(s.grad.cpu(), s2.grad.cpu()) < 1e-5
+
+    # kv-packed: q (B, Sq, Hq, d) against kv (B, Sk, 2, Hkv, d)
+    sq, sk, hq, hkv = 90, 150, 8, 2
+    q0 = torch.randn(B, sq, hq, d, generator=g).to(torch.bfloat16)
+    kv0 = torch.randn(B, sk, 2, hkv, d, generator=g).to(torch.bfloat16)
+    s3 = torch.randn(hq, generator=g, dtype=torch.float32)
+    do3 = torch.randn(B, sq, hq, d, generator=g).to(torch.bfloat16).cuda()
+    q, kv, s = _leaf(q0), _leaf(kv0), _leaf(s3)
+    out = ext.attn_sink_kvpacked_func(q, kv, learnable_sink=s)
+    out.backward(do3)
+    q2, kv2, s2 = _leaf(q0.reshape(B * sq, hq, d)), _leaf(kv0.reshape(B * sk, 2, hkv, d)), _leaf(s3)
+    cq = torch.arange(0, (B + 1) * sq, sq, dtype=torch.int32, device="cuda")
+    ck = torch.arange(0, (B + 1) * sk, sk, dtype=torch.int32, device="cuda")
+    out2 = ext.attn_sink_varlen_kvpacked_func(q2, kv2, cq, ck, sq, sk, learnable_sink=s2)
+    out2.backward(do3.reshape(B * sq, hq, d))
+    torch.cuda.synchronize()
+    assert ext.device_status() == 0
+    assert torch.equal(out.detach().reshape(B * sq, hq, d), out2.detach())
+    assert torch.equal(kv.grad.reshape(B * sk, 2, hkv, d), kv2.grad)
+    assert rel_fro(q.grad.reshape(B * sq, hq, d).cpu(), q2.grad.cpu()) < 1e-5
+    # and the packed forward is the unpacked one, bit for bit
+    k_, v_ = kv0.reshape(B * sk, 2, hkv, d)[:, 0].contiguous(), kv0.reshape(B * sk, 2, hkv, d)[:, 1].contiguous()
+    ref, _ = ext.attn_sink_fwd(q0.reshape(B * sq, hq, d).cuda(), k_.cuda(), v_.cuda(), s3.cuda(), cq, ck, sq, sk)
+    assert torch.equal(out2.detach(), ref)
