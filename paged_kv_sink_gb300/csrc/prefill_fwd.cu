@@ -415,12 +415,22 @@ __global__ void __launch_bounds__(kThreads, 2)
             // the tensor core during this tile's whole exp2 phase; P is computed and
             // stored in two halves, the first half's TMEM store overlapping the
             // second half's exp2 work.
+            // The second half of S is still loading while the first half is
+            // exponentiated; S is released once both halves are in registers.
             uint32_t s[4][32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
+            tmem_ld32(tS, s[0]);
+            tmem_ld32(tS + 32, s[1]);
             tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(&S.s_free);
+            tmem_ld32(tS + 64, s[2]);
+            tmem_ld32(tS + 96, s[3]);
+            bool s_in = false;
+            auto finish_s_load = [&]() {
+                if (s_in) return;
+                s_in = true;
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(&S.s_free);
+            };
 
             const int jmax = j0 + BN - 1;
             const bool full = (!p.causal || jmax <= P0) && (jmax < Lk) &&
@@ -491,6 +501,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (!slow) {
                 if (!full) mask_half(H0{});
                 const float rs0 = exps_half(H0{}, m_ref);
+                finish_s_load();
                 const bool ok0 = !__any_sync(0xffffffffu, !(rs0 <= kFastSumLimit));
                 if (!(ok = wait_prev_pv())) break;
                 if (ok0) {
@@ -507,6 +518,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     slow = true;
                 }
             } else {
+                finish_s_load();
                 if (!full) {
                     mask_half(H0{});
                     mask_half(H1{});
