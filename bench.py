@@ -39,14 +39,14 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # Keyed by kernel + workload; each entry records the hash of the kernel source
 # it was measured on and is reported only while that source is unchanged.
 NCU_TRAFFIC = {
-    # fwd_kernel<64>: 442.4 MB read + 259.1 MB written per launch
-    "fwd_kernel/extend_varlen": {"src": "eb307af008e5bef1", "bytes": 701_490_176},
-    # fwd_kernel<64>, first 1024 + last 7168 window: 488.2 MB + 268.2 MB
-    "fwd_kernel/extend_window": {"src": "eb307af008e5bef1", "bytes": 756_366_592},
-    # fwd_kernel<64> reading K/V through a page-16 table: 445.7 MB + 258.7 MB
-    "fwd_kernel/extend_paged": {"src": "eb307af008e5bef1", "bytes": 704_400_640},
-    # fwd2_kernel<128> (two query heads per CTA): 1006.9 MB + 272.9 MB
-    "fwd_kernel/extend_d128": {"src": "eb307af008e5bef1", "bytes": 1_279_807_232},
+    # fwd_kernel<64>: 443.6 MB read + 258.8 MB written per launch
+    "fwd_kernel/extend_varlen": {"src": "01113da51d930ad5", "bytes": 702_400_512},
+    # fwd_kernel<64>, first 1024 + last 7168 window: 488.6 MB + 267.9 MB
+    "fwd_kernel/extend_window": {"src": "01113da51d930ad5", "bytes": 756_435_968},
+    # fwd_kernel<64> reading K/V through a page-16 table: 445.6 MB + 258.6 MB
+    "fwd_kernel/extend_paged": {"src": "01113da51d930ad5", "bytes": 704_219_904},
+    # fwd2_kernel<128> (two query heads per CTA): 998.5 MB + 272.9 MB
+    "fwd_kernel/extend_d128": {"src": "01113da51d930ad5", "bytes": 1_271_381_504},
     # bwd_main_kernel<64>: 2.684 GB read + 1.048 GB written per launch
     "bwd_main_kernel/train": {"src": "8450e18315e5943f", "bytes": 3_731_941_632},
     # bwd_main128_kernel on the head-dim-128 training step: 1.910 GB + 0.946 GB

@@ -411,12 +411,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                 break;
             }
             tc_fence_after();
-            // S is read into registers and released at once, so the next S runs on
-            // the tensor core during this tile's whole exp2 phase; P is computed and
-            // stored in two halves, the first half's TMEM store overlapping the
-            // second half's exp2 work.
-            // The second half of S is still loading while the first half is
-            // exponentiated; S is released once both halves are in registers.
+            // S is read into registers and released as soon as all of it is in: the
+            // second half is still loading while the first half is exponentiated, and
+            // the next S runs on the tensor core during the rest of the exp2 phase.  P
+            // is computed and stored in two halves, the first half's TMEM store
+            // overlapping the second half's exp2 work.
             uint32_t s[4][32];
             tmem_ld32(tS, s[0]);
             tmem_ld32(tS + 32, s[1]);
@@ -892,10 +891,10 @@ __global__ void __launch_bounds__(x2::kThreads, 1)
                 break;
             }
             tc_fence_after();
-            // S is read into registers and released at once, so the next S runs on
-            // the tensor core during this tile's whole exp2 phase; P is computed and
-            // stored in two halves, the first half's TMEM store overlapping the
-            // second half's exp2 work.
+            // S is read into registers; P is computed and stored over it in two
+            // halves, the first half's TMEM store overlapping the second half's exp2
+            // work.  This tile's next S is issued once its P V has read P, and in the
+            // meantime the tensor core runs the other tile's products.
             uint32_t s[4][32];
 #pragma unroll
             for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
