@@ -47,6 +47,10 @@
  *  - Out-of-range page ids and sequence lengths longer than the page table
  *    are caught on the device: the offending load is skipped and a sticky
  *    device status is set, which attn_sink_device_status() reports.
+ *  - One call takes at most 65535 requests (batch) in the forward, paged
+ *    forward, decode and append entry points, and at most 65535 * 128 query
+ *    rows per request in the forward ones (each is one grid dimension of the
+ *    launch); larger calls return ATTN_SINK_ERR_UNSUPPORTED.
  */
 #ifndef ATTN_SINK_H
 #define ATTN_SINK_H
@@ -62,7 +66,7 @@ typedef uint16_t attn_bf16;
 enum {
     ATTN_SINK_OK = 0,
     ATTN_SINK_ERR_INVALID = -1,      /* NULL pointer, negative size, bad flag combination */
-    ATTN_SINK_ERR_UNSUPPORTED = -2,  /* head_dim, group size or page_size not supported   */
+    ATTN_SINK_ERR_UNSUPPORTED = -2,  /* head_dim, group size, page_size or a size limit   */
     ATTN_SINK_ERR_CUDA = -3,         /* a CUDA call failed (allocation, launch)            */
     ATTN_SINK_ERR_DEVICE = -4        /* a device-side check failed (see device_status)     */
 };

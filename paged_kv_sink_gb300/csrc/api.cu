@@ -35,6 +35,19 @@ int cuda_fail(cudaError_t e, const char* what) {
     return fail(ATTN_SINK_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
 }
 
+// The forward, decode and append grids give the request index a grid dimension
+// of at most 65535 blocks, and the forward its 128-row query tiles another.
+constexpr int kMaxGridDim = 65535;
+
+int check_grid(const char* who, int batch, int max_seqlen_q) {
+    if (batch > kMaxGridDim)
+        return fail(ATTN_SINK_ERR_UNSUPPORTED, "%s: batch %d above %d requests per call", who, batch, kMaxGridDim);
+    if (max_seqlen_q > 0 && (max_seqlen_q + 127) / 128 > kMaxGridDim)
+        return fail(ATTN_SINK_ERR_UNSUPPORTED, "%s: max_seqlen_q %d above %d query rows per request", who,
+                    max_seqlen_q, kMaxGridDim * 128);
+    return ATTN_SINK_OK;
+}
+
 // One library-owned stream-ordered memory pool per device.  Freed blocks are
 // kept (release threshold = max) so that steady-state calls do not go back to
 // the driver.
@@ -122,7 +135,7 @@ int validate_decode(const char* who, const attn_bf16* q, const attn_bf16* k_cach
         return fail(ATTN_SINK_ERR_INVALID, "%s: q, caches and out must be 16-byte aligned", who);
     if ((long long)num_pages * page_size >= (1LL << 31) || (long long)max_pages * page_size >= (1LL << 31))
         return fail(ATTN_SINK_ERR_UNSUPPORTED, "%s: cache slots must fit in int32", who);
-    return ATTN_SINK_OK;
+    return check_grid(who, batch, 0);
 }
 
 }  // namespace attn
@@ -222,6 +235,7 @@ int attn_sink_kv_append(const attn_bf16* k_new, const attn_bf16* v_new, const in
         return fail(ATTN_SINK_ERR_INVALID, "kv_append: tensors must be 16-byte aligned");
     if (!cu_new && max_new != 1)
         return fail(ATTN_SINK_ERR_INVALID, "kv_append: without cu_new every request appends one row (max_new 1)");
+    if (int rc = check_grid("kv_append", batch, 0)) return rc;
     return run_append(k_new, v_new, cu_new, seqlens, page_table, max_pages, batch, hkv, head_dim, page_size,
                       num_pages, max_new, k_cache, v_cache, static_cast<cudaStream_t>(stream));
 }
@@ -317,6 +331,7 @@ int fwd_impl(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, long lo
     int rc = validate_varlen("fwd", q, k, v, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, hq, hkv, head_dim,
                              max_seqlen_q, max_seqlen_k, win_first, win_last, causal, true);
     if (rc != ATTN_SINK_OK || batch == 0 || max_seqlen_q == 0 || total_q == 0) return rc;
+    if ((rc = check_grid("fwd", batch, max_seqlen_q)) != ATTN_SINK_OK) return rc;
     if (!out) return fail(ATTN_SINK_ERR_INVALID, "fwd: NULL out");
     if (!aligned16(out)) return fail(ATTN_SINK_ERR_INVALID, "fwd: out must be 16-byte aligned");
     attn::prefill::FwdArgs a = {};
@@ -458,6 +473,7 @@ int attn_sink_fwd_paged(const attn_bf16* q, const attn_bf16* k_new, const attn_b
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
         (k_new && (!aligned16(k_new) || !aligned16(v_new))))
         return fail(ATTN_SINK_ERR_INVALID, "fwd_paged: tensors must be 16-byte aligned");
+    if (int rc = check_grid("fwd_paged", batch, max_seqlen_q)) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (k_new) {
         int rc = run_append(k_new, v_new, cu_seqlens_q, seqlens_k, page_table, max_pages, batch, hkv, head_dim,

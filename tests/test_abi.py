@@ -135,6 +135,25 @@ def test_validation_of_the_extended_entry_points_without_gpu(lib):
     assert fwd_host([0, 0, 0], [0, 7, 9], 2) == 0  # no query rows: nothing to do
 
 
+def test_grid_limits_rejected_on_the_host(lib):
+    """More requests (or query rows per request) than a launch grid dimension
+    holds come back as -2 with a message, before any CUDA work."""
+    P = ctypes.c_void_p(16)  # never dereferenced: validation fails first
+    # forward: 65536 requests; then one request of 65535 * 128 + 1 query rows
+    rc = lib.attn_sink_fwd(P, P, P, None, P, P, 65536, 1, 1, 4, 2, 64, 1, 1, 0, 0, 1, 0.0, P, None, None)
+    assert rc == -2 and b"batch" in lib.attn_sink_last_error()
+    rc = lib.attn_sink_fwd(P, P, P, None, P, P, 1, 1, 1, 4, 2, 64, 65535 * 128 + 1, 1, 0, 0, 1, 0.0, P, None, None)
+    assert rc == -2 and b"max_seqlen_q" in lib.attn_sink_last_error()
+    rc = lib.attn_sink_fwd(P, P, P, None, P, P, 65535, 1, 1, 4, 2, 64, 65535 * 128, 1, 0, 0, 1, 0.0, None, None,
+                           None)
+    assert rc == -1 and b"out" in lib.attn_sink_last_error()  # at the limits: on to the next check
+    # decode and append: 65536 requests
+    rc = lib.attn_sink_decode_paged(P, P, P, P, 4, P, 65536, 8, 2, 64, 16, 4, None, 0, 0, 0.0, P, None, None)
+    assert rc == -2 and b"batch" in lib.attn_sink_last_error()
+    rc = lib.attn_sink_kv_append(P, P, None, P, P, 4, 65536, 2, 64, 16, 8, 1, P, P, None)
+    assert rc == -2 and b"batch" in lib.attn_sink_last_error()
+
+
 def test_autograd_functions_check_arguments_on_the_host(lib):
     """The autograd functions only marshal arguments: host tensors and
     malformed shapes are rejected before any library call."""
