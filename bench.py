@@ -51,10 +51,10 @@ NCU_TRAFFIC = {
     "bwd_main_kernel/train": {"src": "8450e18315e5943f", "bytes": 3_731_941_632},
     # bwd_main128_kernel on the head-dim-128 training step: 1.910 GB + 0.946 GB
     "bwd_main128_kernel/train_d128": {"src": "8450e18315e5943f", "bytes": 2_856_080_128},
-    # decode_split_kernel: 1.943 GB + 0.011 GB
-    "decode/decode_sink": {"src": "c0d40bc40087f07f", "bytes": 1_954_153_216},
+    # decode_split_kernel: 1.943 GB + 0.010 GB
+    "decode/decode_sink": {"src": "5bc7ecc88224f35a", "bytes": 1_953_821_440},
     # decode_split_kernel: 1.074 GB + 0.007 GB
-    "decode/decode_window": {"src": "c0d40bc40087f07f", "bytes": 1_081_029_120},
+    "decode/decode_window": {"src": "5bc7ecc88224f35a", "bytes": 1_080_700_928},
 }
 
 

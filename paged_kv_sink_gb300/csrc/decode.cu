@@ -118,6 +118,11 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitParam
     __shared__ uint8_t row_ok[NSTAGE][kChunk];
     constexpr int kStageBytes = 2 * kChunk * D * 2;
     constexpr int kSegs = D / 8;                        // 16-byte segments per row
+    // The combine kernel is launched as a programmatic dependent of this grid:
+    // once every CTA of this grid has started, its CTAs may be scheduled, and
+    // they wait (griddepcontrol.wait) for this grid to finish before reading
+    // the partials.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     const int split = blockIdx.x;
     const int kvh = blockIdx.y / p.hblocks;
@@ -347,6 +352,9 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const SplitParams p, 
     const int nsplit = (int)(((long long)nvis + p.split_tokens - 1) / p.split_tokens);
     const size_t base = ((size_t)b * p.hq + h) * p.max_splits;
     const float sg = sink ? sink[h] * ATTN_LOG2E : -INFINITY;
+    // the split grid (this launch's programmatic predecessor) has completed and
+    // its partials are visible past this point
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     float M = sg;
     for (int s = 0; s < nsplit; ++s) M = fmaxf(M, p.part_ml[base + s].x);
     float o = 0.f, lse_v;
@@ -493,12 +501,26 @@ cudaError_t launch(const Args& a, const Plan& pl, float* part_o, float2* part_ml
         e = pl.nt == 1 ? launch_split<128, 1, 3>(sp, pl, a.batch, a.hkv, s)
                        : launch_split<128, 2, 3>(sp, pl, a.batch, a.hkv, s);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.hq, a.batch);
+    // The combine starts as a programmatic dependent of the split grid: its
+    // launch and CTA set-up overlap the split kernel's last wave.
     auto* out = reinterpret_cast<__nv_bfloat16*>(a.out);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.hq, a.batch);
+    cfg.blockDim = dim3(a.head_dim == 64 ? 64 : 128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const float* sink = a.sink;
+    float* lse = a.lse;
     if (a.head_dim == 64)
-        decode_combine_kernel<64><<<grid, 64, 0, s>>>(sp, a.sink, out, a.lse);
+        e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<64>, sp, sink, out, lse);
     else
-        decode_combine_kernel<128><<<grid, 128, 0, s>>>(sp, a.sink, out, a.lse);
+        e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<128>, sp, sink, out, lse);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
